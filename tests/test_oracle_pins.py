@@ -1,0 +1,369 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+* brute force on tiny rows: every subset of the right size is tried and the
+  one that dominates the rest under (score desc, column asc) must be the
+  oracle's (a different mechanism from the oracle's full sort);
+* the score-multiset property on realistic rows (numpy sort of reals);
+* the hand-worked B' pack table (tests/golden/pack_example.txt);
+* the closed form of the pairs merge: the top-K of the union of every rank's
+  logits (the merge only sees each rank's top-K list);
+* hand-worked saturation / rescue example;
+* the decode-merge exactness invariant and the saturation rows of a skewed
+  workload;
+* the checkers bite: corrupted outputs fail them.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from checks import (bf16_bits_to_f32, check_decode_merge_row, check_topk_layout,
+                    check_topk_row, order_key, packed_contract)
+from sparse_attention_indexer_radix_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+ALPHABET = [math.nan, -math.inf, -1.0, -0.0, 0.0, 1.0, math.inf]
+
+
+def brute_topk(vals, end, k):
+    """All subsets of size min(k, n_valid): the answer is the one whose
+    every member strictly precedes every non-member under (score desc,
+    column asc).  Laid out as [> K-th, by column][== K-th, by column]; a
+    short row is all valid columns by column."""
+    valid = [c for c in range(end) if not math.isnan(vals[c])]
+
+    def before(a, b):  # a strictly precedes b
+        ka, kb = order_key(vals[a]), order_key(vals[b])
+        return ka > kb or (ka == kb and a < b)
+
+    m = min(k, len(valid))
+    winners = []
+    for sub in itertools.combinations(valid, m):
+        s = set(sub)
+        if all(before(a, b) for a in sub for b in valid if b not in s):
+            winners.append(sub)
+    assert len(winners) == 1
+    chosen = list(winners[0])
+    if len(valid) < k:
+        return sorted(chosen) + [-1] * (k - len(valid))
+    kth = min((order_key(vals[c]) for c in chosen))
+    gt = sorted(c for c in chosen if order_key(vals[c]) > kth)
+    eq = sorted(c for c in chosen if order_key(vals[c]) == kth)
+    return gt + eq
+
+
+def test_topk_exhaustive_tiny_alphabet():
+    L = 4
+    rows = np.array(list(itertools.product(ALPHABET, repeat=L)), dtype=np.float32)
+    for k in range(1, L + 2):
+        for end in range(0, L + 1):
+            ends = np.full(len(rows), end, dtype=np.int32)
+            got = oracle.topk_rows(rows, k, row_ends=ends)
+            for i in range(len(rows)):
+                want = brute_topk(rows[i].tolist(), end, k)
+                assert got[i].tolist() == want, (rows[i], end, k, got[i], want)
+
+
+def test_topk_random_small_rows_few_levels():
+    rng = np.random.default_rng(7)
+    levels = np.array([math.nan, -math.inf, -2.5, -1.0, -0.0, 0.0, 0.5, 1.0, 3.0,
+                       math.inf], dtype=np.float32)
+    for cols in (5, 8, 12):
+        x = levels[rng.integers(0, len(levels), size=(300, cols))]
+        ends = rng.integers(-2, cols + 3, size=300).astype(np.int32)
+        for k in (1, 2, 3, cols // 2, cols, cols + 1):
+            got = oracle.topk_rows(x, k, row_ends=ends)
+            for i in range(len(x)):
+                e = max(0, min(int(ends[i]), cols))
+                assert got[i].tolist() == brute_topk(x[i].tolist(), e, k)
+
+
+def test_topk_signed_zero_and_infinities():
+    x = np.array([[-0.0, 0.0], [0.0, -0.0]], dtype=np.float32)
+    assert oracle.topk_rows(x, 1).tolist() == [[1], [0]]
+    assert oracle.topk_rows(x, 2).tolist() == [[1, 0], [0, 1]]
+    y = np.array([[-math.inf, math.nan, math.inf, 5.0, -math.inf]], dtype=np.float32)
+    assert oracle.topk_rows(y, 2).tolist() == [[2, 3]]
+    assert oracle.topk_rows(y, 4).tolist() == [[2, 3, 0, 4]]
+    assert oracle.topk_rows(y, 3).tolist() == [[2, 3, 0]]
+    allnan = np.full((1, 9), math.nan, dtype=np.float32)
+    assert oracle.topk_rows(allnan, 4).tolist() == [[-1, -1, -1, -1]]
+
+
+def test_topk_prefill_smoke_shape_scores_and_layout():
+    x, ends = inputs.prefill(rows=64, cols=4096, seed=1235)
+    x, ends = x.numpy(), ends.numpy()
+    out = np.full((64, 640), -7, dtype=np.int32)
+    oracle.topk_rows(x, 512, row_ends=ends, out=out)
+    for i in range(64):
+        e = int(ends[i])
+        check_topk_row(x[i], e, 512, out[i], ld_canary=-7, where=f"row {i}")
+        check_topk_layout(x[i], e, 512, out[i], where=f"row {i}")
+        # N(0,1) fp32 rows have no ties at the cut: the set is argsort's
+        want = set(np.argsort(-x[i, :e], kind="stable")[:512].tolist())
+        assert set(out[i, :512].tolist()) == want
+
+
+def test_topk_bf16_agrees_with_widened_f32():
+    x, ends, _ = inputs.adversarial(rows=12, cols=3000, seed=99)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    f = bf16_bits_to_f32(bits)
+    e = ends.numpy()
+    for k in (1, 17, 600, 2048):
+        a = oracle.topk_rows(bits, k, row_ends=e)
+        b = oracle.topk_rows(f, k, row_ends=e)
+        assert np.array_equal(a, b)
+        for i in range(12):
+            end = max(0, min(int(e[i]), 3000))
+            check_topk_row(f[i], end, k, a[i], where=f"k={k} row {i}")
+            check_topk_layout(f[i], end, k, a[i], where=f"k={k} row {i}")
+
+
+def test_topk_short_rows_tails_and_padding():
+    x, _ = inputs.prefill(rows=8, cols=100, seed=5)
+    x = x.numpy()
+    ends = np.array([0, 1, 5, 31, 32, 33, 100, 1000], dtype=np.int32)
+    out = np.full((8, 48), 12345, dtype=np.int32)
+    oracle.topk_rows(x, 32, row_ends=ends, out=out)
+    for i in range(8):
+        e = max(0, min(int(ends[i]), 100))
+        check_topk_row(x[i], e, 32, out[i], ld_canary=12345)
+        n = min(32, e)
+        assert np.all(out[i, n:32] == -1)
+
+
+# ------------------------------------------------------------------ pack --
+
+def _load_pack_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "pack_example.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            j, bits, local, whex, wint, plane, gid = line.split()
+            rows.append(dict(j=int(j), bits=None if bits == "-" else int(bits, 16),
+                             local=int(local), word=int(wint), plane=int(plane),
+                             gid=None if gid == "-" else int(gid)))
+    return rows
+
+
+def _pack_golden_inputs():
+    g = _load_pack_golden()
+    S = (1 << 17) + 1
+    logits = np.zeros((1, S), dtype=np.uint16)
+    idx = np.full((1, 32), -1, dtype=np.int32)
+    for e in g:
+        idx[0, e["j"]] = e["local"]
+        if e["bits"] is not None:
+            logits[0, e["local"]] = e["bits"]
+    return g, logits, idx, S
+
+
+def test_pack_hand_worked_example():
+    g, logits, idx, S = _pack_golden_inputs()
+    packed = oracle.dcp_pack(logits, idx, row_ends=np.array([S], dtype=np.int32))
+    want = np.zeros(33, dtype=np.int32)
+    for e in g:
+        want[e["j"]] = e["word"]
+    want[32] = 0x22
+    assert packed[0].tolist() == want.tolist()
+    # decode through the merge: owner rank 3 of W = 8, others empty
+    W, k = 8, 64
+    gathered = np.zeros((W, 1, 33), dtype=np.int32)
+    gathered[3, 0] = packed[0]
+    ids, sat, status = oracle.merge_packed(gathered, k)
+    chosen = [e["gid"] for e in g if e["gid"] is not None]
+    assert ids[0, :len(chosen)].tolist() == chosen
+    assert np.all(ids[0, len(chosen):] == -1)
+
+
+def test_bf16_order_chain_through_pack():
+    """-inf < -max < -1 < -0 < +0 < 1 < max < +inf, through the words."""
+    chain = [0xFF80, 0xFF7F, 0xBF80, 0x8000, 0x0000, 0x3F80, 0x7F7F, 0x7F80]
+    want_ord = [0x007F, 0x0080, 0x407F, 0x7FFF, 0x8000, 0xBF80, 0xFF7F, 0xFF80]
+    logits = np.array([chain], dtype=np.uint16)
+    idx = np.array([list(range(8)) + [-1] * 24], dtype=np.int32)
+    w = oracle.dcp_pack(logits, idx)[0, :8].astype(np.int64) & 0xFFFFFFFF
+    assert (w >> 16).tolist() == want_ord
+    assert ((0xFFFF - (w & 0xFFFF))).tolist() == list(range(8))
+
+
+def test_pack_contract_on_local_topn():
+    lg, _, _ = inputs.decode_merge(W=2, rows=6, S=3000, n=64, k=256, skew_count=80, seed=3)
+    bits = lg.view(torch.int16).numpy().view(np.uint16).reshape(12, 3000)
+    ends = np.array([3000, 10, 64, 65, 2999, 0] * 2, dtype=np.int32)
+    local = oracle.topk_rows(bits, 64, row_ends=ends)
+    packed = oracle.dcp_pack(bits, local, row_ends=ends)
+    packed_contract(packed, bits, ends, 64)
+
+
+def test_pack_drops_out_of_range_and_nan():
+    S = 100
+    logits = np.full((1, S), 0x3F80, dtype=np.uint16)
+    logits[0, 4] = 0x7FC1
+    idx = np.array([[-5, 0, 4, 99, 100, 50, 2**17, 7] + [-1] * 24], dtype=np.int32)
+    p = oracle.dcp_pack(logits, idx, row_ends=np.array([60], dtype=np.int32))
+    nz = (p[0, :32] != 0).tolist()
+    assert nz[:8] == [False, True, False, False, False, True, False, True]
+
+
+# ----------------------------------------------------------------- merges --
+
+def test_pairs_merge_equals_union_topk():
+    W, R, k, local = 8, 24, 256, 2048
+    cand, logits = inputs.pairs_merge(W=W, rows=R, k=k, local=local, seed=11, keep_logits=True)
+    cand_np = cand.numpy()
+    ids = oracle.merge_pairs(cand_np, k)
+    lg = logits.numpy()
+    for t in range(R):
+        scores = lg[:, t, :].reshape(-1)           # [W * local], rank-major
+        r = np.repeat(np.arange(W), local)
+        loc = np.tile(np.arange(local), W)
+        gid = loc * W + r
+        order = np.lexsort((gid, -scores))
+        want = set(gid[order[:k]].tolist())
+        assert set(ids[t].tolist()) == want
+        # flat-order layout: chosen positions ascend in the rank-major buffer
+        flat_of = {}
+        for rr in range(W):
+            for j in range(k):
+                flat_of[int(cand_np[rr, t, j, 1])] = rr * k + j
+        pos = [flat_of[g] for g in ids[t].tolist()]
+        assert pos == sorted(pos)
+
+
+def test_pairs_merge_empty_entries_and_short():
+    W, k, n = 2, 8, 4
+    cand = np.zeros((W, 1, n, 2), dtype=np.int32)
+    sc = np.array([[3.0, np.nan, 1.0, 2.0], [5.0, 0.5, -1.0, 7.0]], dtype=np.float32)
+    gid = np.array([[0, 2, -1, 6], [1, 3, 5, 7]], dtype=np.int32)
+    cand[:, 0, :, 0] = sc.view(np.int32)
+    cand[:, 0, :, 1] = gid
+    ids = oracle.merge_pairs(cand, k)
+    # valid: (3,0) (2,6) (5,1) (0.5,3) (-1,5) (7,7); fewer than k -> all, flat order
+    assert ids[0].tolist() == [0, 6, 1, 3, 5, 7, -1, -1]
+    ids3 = oracle.merge_pairs(cand, 3)
+    assert ids3[0].tolist() == [0, 1, 7]
+
+
+def _hand_rescue_case():
+    """W=2, n=32, K=64, S=64.  Rank 0 scores 200-l, rank 1 scores 100-l
+    (exact in bf16).  Round 1 sees rank 0's top-32 and rank 1's top-32; the
+    K-th is 69, rank 0 is saturated, the rescue must return rank 0's 64."""
+    W, T, S, n, k = 2, 1, 64, 32, 64
+    vals = np.zeros((W, T, S), dtype=np.float32)
+    vals[0, 0] = 200.0 - np.arange(S)
+    vals[1, 0] = 100.0 - np.arange(S)
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    return W, T, S, n, k, bits
+
+
+def test_rescue_hand_worked_example():
+    W, T, S, n, k, bits = _hand_rescue_case()
+    local = oracle.topk_rows(bits.reshape(W * T, S), n)
+    packed = oracle.dcp_pack(bits.reshape(W * T, S), local).reshape(W, T, n + n // 32)
+    ids, sat, status = oracle.merge_packed(packed, k)
+    assert status == 0
+    # round 1: rank 0 locals 0..31 (gid 2l), rank 1 locals 0..31 (gid 2l+1)
+    assert ids[0].tolist() == [2 * l for l in range(32)] + [2 * l + 1 for l in range(32)]
+    assert sat[0] == (1 << 16) | 0xC28A  # mask 0b01, tau16 = ord16(bf16 69.0)
+    ids2, recv, status = oracle.rescue(packed, k, bits, sat, ids.copy())
+    assert status == 0
+    assert ids2[0].tolist() == [2 * l for l in range(64)]
+    words = recv[0, 0, :64].astype(np.int64) & 0xFFFFFFFF
+    assert ((0xFFFF - (words & 0xFFFF))).tolist() == list(range(64))
+    check_decode_merge_row(ids2[0], bits, 0, k)
+
+
+def _decode_pipeline(W, T, S, n, k, skew_count, seed):
+    lg, skewed, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, skew_count=skew_count,
+                                        seed=seed)
+    bits = lg.view(torch.int16).numpy().view(np.uint16)
+    flat = bits.reshape(W * T, S)
+    local = oracle.topk_rows(flat, n)
+    packed = oracle.dcp_pack(flat, local).reshape(W, T, n + n // 32)
+    ids1, sat, status = oracle.merge_packed(packed, k)
+    ids2, recv, status2 = oracle.rescue(packed, k, bits, sat, ids1.copy())
+    return bits, skewed.numpy(), packed, ids1, sat, ids2, recv, status | status2
+
+
+def test_decode_merge_exact_and_saturation_rows():
+    W, T, S, n, k = 8, 16, 4096, 96, 512
+    bits, skewed, packed, ids1, sat, ids2, recv, status = _decode_pipeline(
+        W, T, S, n, k, skew_count=150, seed=21)
+    assert status == 0
+    mask = (sat.astype(np.int64) & 0xFFFFFFFF) >> 16
+    assert np.array_equal(mask != 0, skewed), (mask, skewed)
+    for t in range(T):
+        check_decode_merge_row(ids2[t], bits, t, k, where="rescued")
+    bitten = 0
+    for t in np.nonzero(skewed)[0]:
+        try:
+            check_decode_merge_row(ids1[t], bits, t, k)
+        except AssertionError:
+            bitten += 1
+    assert bitten >= 1, "round 1 alone should miss tokens on a skewed row"
+    for t in np.nonzero(~skewed)[0]:
+        assert np.array_equal(ids1[t], ids2[t])
+
+
+def test_decode_merge_deterministic():
+    a = _decode_pipeline(4, 6, 2048, 64, 256, skew_count=80, seed=5)
+    b = _decode_pipeline(4, 6, 2048, 64, 256, skew_count=80, seed=5)
+    for x, y in zip(a[2:7], b[2:7]):
+        assert np.array_equal(x, y)
+
+
+def test_packed_merge_duplicate_words_out_of_contract():
+    """A producer that repeats a word (a NaN row's arbitrary ids, on the
+    page) is outside the contract: the select keeps fewer than K rather than
+    reading past, reports it, and tau16 falls to 0."""
+    W, n, k = 1, 32, 4
+    packed = np.zeros((W, 1, 33), dtype=np.int32)
+    w = (0xBF80 << 16) | (0xFFFF - 3)
+    packed[0, 0, :6] = np.array([w, w, w, w, w, w], dtype=np.uint32).view(np.int32)
+    ids, sat, status = oracle.merge_packed(packed, k)
+    assert status & 2
+    assert ids[0].tolist() == [-1, -1, -1, -1]
+    assert (int(sat[0]) & 0xFFFF) == 0
+
+
+# ------------------------------------------------------- checkers bite --
+
+def test_checkers_reject_corrupted_outputs():
+    x, ends = inputs.prefill(rows=4, cols=600, seed=8)
+    x, ends = x.numpy(), ends.numpy()
+    out = oracle.topk_rows(x, 64, row_ends=ends)
+    e = int(ends[0])
+    bad = out[0].copy()
+    # swap a chosen id for an unchosen lower-scoring column
+    unchosen = [c for c in np.argsort(x[0, :e]) if c not in set(bad.tolist())]
+    bad[5] = unchosen[0]
+    with pytest.raises(AssertionError):
+        check_topk_row(x[0], e, 64, bad)
+    bad = out[0].copy()
+    bad[[3, 4]] = bad[[4, 3]]
+    with pytest.raises(AssertionError):
+        check_topk_layout(x[0], e, 64, bad)
+    bad = out[0].copy()
+    bad[10] = bad[11]
+    with pytest.raises(AssertionError):
+        check_topk_row(x[0], e, 64, bad)
+
+
+def test_contract_checker_bites():
+    lg, _, _ = inputs.decode_merge(W=1, rows=2, S=500, n=32, k=64, skew_count=10, seed=4)
+    bits = lg.view(torch.int16).numpy().view(np.uint16).reshape(2, 500)
+    local = oracle.topk_rows(bits, 32)
+    worst = np.argsort(bf16_bits_to_f32(bits[0]))[0]
+    local[0, 0] = worst  # a sent token below an unsent one
+    packed = oracle.dcp_pack(bits, local)
+    with pytest.raises(AssertionError):
+        packed_contract(packed, bits, None, 32)
