@@ -1,0 +1,214 @@
+// dcp_rescue.cu -- satk_dcp_rescue_select: the second round of the packed
+// merge (vLLM API page vllm.models.kimi_k3.nvidia.ops.dcp_topk_merge
+// .kernels: module docstring, push_local_topk inside DCPTopkSelectKernel,
+// DCPTopkRescueKernel).
+//
+// On the page each saturated rank pushes its local top-K into every rank's
+// receive slot with peer stores and a release flag, and a persistent kernel
+// spins on the flags before re-selecting.  Here all W ranks' rows are in
+// one device buffer, so the push is an ordinary kernel writing `recv` and
+// stream order replaces the flags: nothing waits on anything.
+//
+// rescue_push_kernel  : one CTA per (row, slot); slot s of a row with a
+//                       non-zero mask takes the s-th set bit's rank, runs the
+//                       row top-K on that rank's bf16 logits (the streaming
+//                       path of satk_rows.cuh) and writes the list in the B'
+//                       layout to recv[t, s].
+// rescue_select_kernel: one CTA per row; a zero mask costs one load.  The
+//                       candidates are the round-1 words of the ranks outside
+//                       the mask scoring at or above tau16, then the pushed
+//                       lists; the merge select of satk_merge.cuh picks K.
+#include <climits>
+
+#include "satk_host.hpp"
+#include "satk_merge.cuh"
+#include "satk_rows.cuh"
+
+namespace satk {
+namespace {
+
+constexpr int kPushBlock = 512;
+constexpr int kPushLkpt = 8;
+
+__device__ __forceinline__ int nth_set_bit(uint32_t mask, int s) {
+  for (int q = 0; q < s; ++q) mask &= mask - 1u;
+  return __ffs(mask) - 1;
+}
+
+template <bool VECLOAD>
+__global__ void __launch_bounds__(kPushBlock) rescue_push_kernel(
+    const uint16_t *__restrict__ logits, int64_t S, int64_t ld, int W, int64_t T, int K,
+    int slots, const int32_t *__restrict__ row_ends, const int32_t *__restrict__ sat_word,
+    int32_t *__restrict__ recv, int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  using SM = StreamSmem<kPushBlock, kPushBlock * kPushLkpt>;
+  auto &sm = *reinterpret_cast<SM *>(smem_raw);
+  uint32_t *bp = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SM));
+  const int64_t t = blockIdx.x / slots;
+  const int s = blockIdx.x % slots;
+  const uint32_t mask = static_cast<uint32_t>(sat_word[t]) >> 16;
+  if (mask == 0u) return;
+  const int nsat = __popc(mask);
+  if (nsat > slots || (mask >> W) != 0u) {
+    if (s == 0 && threadIdx.x == 0 && status != nullptr)
+      atomicOr(status, SATK_STATUS_SLOTS_EXCEEDED);
+    return;
+  }
+  if (s >= nsat) return;
+  const int r = nth_set_bit(mask, s);
+  int64_t end = S < SATK_LOCAL_INDEX_LIMIT ? S : SATK_LOCAL_INDEX_LIMIT;
+  if (row_ends != nullptr && (int64_t)row_ends[(int64_t)r * T + t] < end)
+    end = row_ends[(int64_t)r * T + t];
+  if (end < 0) end = 0;
+  const int words = K + K / 32;
+  for (int i = threadIdx.x; i < words; i += kPushBlock) bp[i] = 0u;
+  zero_hist(sm.sel);
+  __syncthreads();
+  topk_stream_row<uint16_t, kPushBlock, kPushLkpt, VECLOAD, true>(
+      logits + ((int64_t)r * T + t) * ld, static_cast<int>(end), K,
+      [&](int pos, uint32_t key, int col) {
+        if ((unsigned)pos >= (unsigned)K) return;
+        bp[pos] = key | (0xffffu - ((uint32_t)col & 0xffffu));
+        if (((uint32_t)col >> 16) & 1u) atomicOr(bp + K + pos / 32, 1u << (pos & 31));
+      },
+      [](int) {}, sm);
+  __syncthreads();
+  int32_t *dst = recv + ((int64_t)t * slots + s) * words;
+  for (int i = threadIdx.x; i < words; i += kPushBlock) dst[i] = static_cast<int32_t>(bp[i]);
+}
+
+template <int BLOCK, int KPT>
+struct RescueSmem {
+  SelectSmem<BLOCK> sel;
+  uint32_t gid[BLOCK * KPT];
+};
+
+template <int BLOCK, int KPT>
+__global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
+    const int32_t *__restrict__ packed, int W, int64_t T, int n, int K, int slots,
+    const int32_t *__restrict__ sat_word, const int32_t *__restrict__ recv,
+    int32_t *__restrict__ ids, int64_t ld_out, int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &sm = *reinterpret_cast<RescueSmem<BLOCK, KPT> *>(smem_raw);
+  const int64_t t = blockIdx.x;
+  const uint32_t sw = static_cast<uint32_t>(sat_word[t]);
+  const uint32_t mask = sw >> 16, tau = sw & 0xffffu;
+  if (mask == 0u) return;  // round 1 was exact
+  const int nsat = __popc(mask);
+  if (nsat > slots || (mask >> W) != 0u) return;  // reported by the push
+  const int lane = lane_id();
+  const int r1 = W * n;
+  const int total = r1 + slots * K;
+  const int words_r1 = n + n / 32, words_k = K + K / 32;
+  zero_hist(sm.sel);
+
+  uint32_t keys[KPT];
+#pragma unroll
+  for (int g = 0; g < KPT; ++g) {
+    const int fb = warp_id() * 32 * KPT + g * 32;
+    uint32_t key = 0u, gid = 0u;
+    if (fb < r1) {
+      const int r = fb / n, j = fb - r * n + lane;
+      if (((mask >> r) & 1u) == 0u) {
+        const int32_t *row = packed + ((int64_t)r * T + t) * words_r1;
+        const uint32_t w = static_cast<uint32_t>(__ldg(row + j));
+        const uint32_t plane = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
+        key = bprime_key(w);
+        if ((key >> 16) < tau) key = 0u;  // below the round-1 cut
+        gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
+      }
+    } else if (fb < total) {
+      const int q = fb - r1;
+      const int s = q / K, j = q - s * K + lane;
+      if (s < nsat) {
+        const int32_t *sl = recv + ((int64_t)t * slots + s) * words_k;
+        const uint32_t w = static_cast<uint32_t>(sl[j]);
+        const uint32_t plane = static_cast<uint32_t>(sl[K + ((j - lane) >> 5)]);
+        key = bprime_key(w);
+        gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)nth_set_bit(mask, s);
+      }
+    }
+    keys[g] = key;
+    sm.gid[fb + lane] = gid;
+  }
+  __syncthreads();
+  int32_t *out = ids + t * ld_out;
+  const MergeOut m = merge_core<BLOCK, KPT, 16>(
+      keys, [&](int i) { return sm.gid[flat_pos<KPT, 1>(i)]; },
+      [&](int pos, int32_t v) {
+        if ((unsigned)pos < (unsigned)K) out[pos] = v;
+      },
+      K, false, sm.sel);
+  if (m.dup && status != nullptr && threadIdx.x == 0)
+    atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
+}
+
+template <int BLOCK, int KPT>
+int launch_rescue_select(const int32_t *packed, int W, int64_t T, int n, int K, int slots,
+                         const int32_t *sat_word, const int32_t *recv, int32_t *ids,
+                         int64_t ld_out, int32_t *status, cudaStream_t st) {
+  auto kern = rescue_select_kernel<BLOCK, KPT>;
+  const size_t smem = sizeof(RescueSmem<BLOCK, KPT>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(T)), BLOCK, smem, st>>>(packed, W, T, n, K, slots, sat_word,
+                                                            recv, ids, ld_out, status);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace satk
+
+extern "C" size_t satk_rescue_recv_words(int64_t T, int32_t n, int32_t k) {
+  if (T < 0 || n < 1 || k < 1) return 0;
+  return static_cast<size_t>(T) * static_cast<size_t>((k - 1) / n) *
+         static_cast<size_t>(k + k / 32);
+}
+
+extern "C" int satk_dcp_rescue_select(const int32_t *packed, int32_t W, int64_t T, int32_t n,
+                                      int32_t k, const uint16_t *logits_bf16, int64_t S,
+                                      int64_t ld_logits, const int32_t *row_ends,
+                                      const int32_t *sat_word, int32_t *recv,
+                                      int32_t *ids_out, int64_t ld_out, int32_t *status,
+                                      satk_stream_t stream) {
+  using namespace satk;
+  if (packed == nullptr || logits_bf16 == nullptr || sat_word == nullptr || recv == nullptr ||
+      ids_out == nullptr || W < 1 || W > 16 || T < 0 || n < 32 || n % 32 != 0 || k < 32 ||
+      k % 32 != 0 || n >= k || k > SATK_TOPK_MAX_K || ld_out < k || S < 0 || ld_logits < S ||
+      T > INT_MAX / 16)
+    return SATK_EINVAL;
+  const int slots = (k - 1) / n;
+  if ((int64_t)W * n + (int64_t)slots * k > SATK_MERGE_MAX_CANDIDATES ||
+      T * slots > INT_MAX)
+    return SATK_EUNSUPPORTED;
+  if (T == 0) return SATK_OK;
+  const cudaStream_t st = as_stream(stream);
+
+  // 1. pushes of the saturated ranks
+  const size_t push_smem = sizeof(StreamSmem<kPushBlock, kPushBlock * kPushLkpt>) +
+                           sizeof(uint32_t) * (size_t)(k + k / 32);
+  const dim3 pgrid(static_cast<unsigned>(T * slots));
+  if (aligned16(logits_bf16) && (ld_logits * 2) % 16 == 0) {
+    auto kern = rescue_push_kernel<true>;
+    if (!allow_smem(kern, push_smem)) return SATK_ECUDA;
+    kern<<<pgrid, kPushBlock, push_smem, st>>>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+                                               sat_word, recv, status);
+  } else {
+    auto kern = rescue_push_kernel<false>;
+    if (!allow_smem(kern, push_smem)) return SATK_ECUDA;
+    kern<<<pgrid, kPushBlock, push_smem, st>>>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+                                               sat_word, recv, status);
+  }
+  int rc = launch_status();
+  if (rc != SATK_OK) return rc;
+
+  // 2. the re-select over round-1 words and the pushed lists
+  const int total = W * n + slots * k;
+  if (total <= 512 * 8)
+    return launch_rescue_select<512, 8>(packed, W, T, n, k, slots, sat_word, recv, ids_out,
+                                        ld_out, status, st);
+  if (total <= 512 * 32)
+    return launch_rescue_select<512, 32>(packed, W, T, n, k, slots, sat_word, recv, ids_out,
+                                         ld_out, status, st);
+  return launch_rescue_select<1024, 32>(packed, W, T, n, k, slots, sat_word, recv, ids_out,
+                                        ld_out, status, st);
+}

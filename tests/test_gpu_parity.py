@@ -1,0 +1,351 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Integer outputs (ids, packed words, saturation words, rescue lists, status
+bits) must match bit for bit.  Cases span several tiles and ragged tails of
+both row paths (register-resident and streaming), fp32 and bf16, aligned and
+unaligned rows, the edge cases of the pages' test plans (empty and short
+rows, rows around K, full rows, strided output with untouched padding, -1
+tails, NaN rows, infinities, signed zeros, massive ties), and the workloads
+at their full sizes (sampled rows where the oracle would be slow)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_indexer_radix_gb300 as satk
+from checks import check_decode_merge_row, check_topk_layout, check_topk_row, packed_contract
+from sparse_attention_indexer_radix_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+CANARY = -7
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_attention_indexer_radix_gb300 import build as satk_build
+    satk_build.build()
+    oracle.build()
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 numpy bit patterns."""
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host_view(x: torch.Tensor) -> np.ndarray:
+    return bits_of(x) if x.dtype == torch.bfloat16 else x.cpu().numpy()
+
+
+def run_topk(x: torch.Tensor, k: int, ends: torch.Tensor | None, ld_out: int, ld_x=None):
+    """GPU and oracle outputs for x ([rows, cols], CPU tensor)."""
+    rows, cols = x.shape
+    if ld_x is not None and ld_x != cols:
+        buf = torch.zeros((rows, ld_x), dtype=x.dtype, device=DEV)
+        buf[:, :cols] = x.to(DEV)
+        xg = buf[:, :cols]
+    else:
+        xg = x.to(DEV)
+    out = torch.full((rows, ld_out), CANARY, dtype=torch.int32, device=DEV)
+    satk.topk_rows(xg, k, row_ends=None if ends is None else ends.to(DEV), out=out)
+    want = np.full((rows, ld_out), CANARY, dtype=np.int32)
+    oracle.topk_rows(host_view(x), k, row_ends=None if ends is None else ends.numpy(), out=want)
+    return out.cpu().numpy(), want
+
+
+def assert_rows_equal(got, want, what=""):
+    if not np.array_equal(got, want):
+        bad = np.nonzero((got != want).any(axis=1))[0]
+        r = int(bad[0])
+        c = np.nonzero(got[r] != want[r])[0][:8]
+        raise AssertionError(f"{what}: {len(bad)} rows differ; row {r} cols {c.tolist()} "
+                             f"got {got[r, c].tolist()} want {want[r, c].tolist()}")
+
+
+# ------------------------------------------------------------- topk_rows --
+
+def test_prefill_smoke_workload():
+    x, ends = inputs.prefill(rows=64, cols=4096, seed=1235)
+    got, want = run_topk(x, 512, ends, 640)
+    assert_rows_equal(got, want, "64x4096 fp32 K=512")
+    for i in range(64):
+        check_topk_row(x[i].numpy(), int(ends[i]), 512, got[i], ld_canary=CANARY)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("cols", [37, 1000, 2048, 2049, 4100, 8191, 8192, 9000, 16390, 40000])
+def test_topk_shapes_both_paths(dtype, cols):
+    rows = 24
+    x, _ = inputs.prefill(rows=rows, cols=cols, seed=cols, dtype=dtype)
+    g = torch.Generator().manual_seed(cols)
+    ends = torch.randint(-3, cols + 5, (rows,), generator=g, dtype=torch.int32)
+    ends[:6] = torch.tensor([0, 1, 511, 512, 513, cols], dtype=torch.int32)
+    for k in (1, 33, 512):
+        got, want = run_topk(x, k, ends, k + 9)
+        assert_rows_equal(got, want, f"{dtype} cols={cols} k={k}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("cols,ld", [(3001, 3003), (20001, 20005), (777, 777)])
+def test_topk_unaligned_rows(dtype, cols, ld):
+    x, ends = inputs.prefill(rows=16, cols=cols, seed=7, dtype=dtype)
+    got, want = run_topk(x, 300, ends, 300, ld_x=ld)
+    assert_rows_equal(got, want, f"unaligned {dtype} cols={cols} ld={ld}")
+
+
+@pytest.mark.parametrize("k", [1, 2047, 2048, 2049, 4096])
+def test_topk_large_k_and_no_row_ends(k):
+    x, _ = inputs.prefill(rows=8, cols=70000, seed=k)
+    got, want = run_topk(x, k, None, k)
+    assert_rows_equal(got, want, f"k={k}")
+
+
+def test_topk_special_values_and_ties():
+    rows, cols = 12, 6000
+    g = torch.Generator().manual_seed(3)
+    levels = torch.tensor([float("-inf"), -2.0, -0.0, 0.0, 1.5, float("inf"), float("nan")])
+    x = levels[torch.randint(0, len(levels), (rows, cols), generator=g)]
+    x[0] = float("nan")                          # all-NaN row
+    x[1] = 1.0                                   # one value everywhere
+    x[2, :] = -0.0
+    x[2, 100:110] = 0.0
+    ends = torch.full((rows,), cols, dtype=torch.int32)
+    for k in (1, 10, 11, 512, 4096):
+        got, want = run_topk(x, k, ends, k + 3)
+        assert_rows_equal(got, want, f"specials k={k}")
+        xb = x.to(torch.bfloat16)
+        got, want = run_topk(xb, k, ends, k + 3)
+        assert_rows_equal(got, want, f"specials bf16 k={k}")
+
+
+@pytest.mark.parametrize("mode", ["plus100", "times1e-8"])
+def test_topk_concentrated_distributions(mode):
+    x, ends = inputs.prefill_shifted(64, 8192, mode)
+    got, want = run_topk(x, 512, ends, 512)
+    assert_rows_equal(got, want, mode)
+    x, ends = inputs.prefill_shifted(16, 51200, mode)
+    got, want = run_topk(x, 512, ends, 512)
+    assert_rows_equal(got, want, mode + " long")
+
+
+def test_adversarial_workload_full():
+    x, ends, nan_row = inputs.adversarial(seed=1239)  # 256 x 131072 bf16, K=2048
+    got, want = run_topk(x, 2048, ends, 2048 + 64)
+    assert_rows_equal(got, want, "adversarial")
+    xb = bits_of(x)
+    f = (xb.astype(np.uint32) << 16).view(np.float32)
+    for i in [0, 1, 2, 3, 4, 5, nan_row]:
+        e = max(0, min(int(ends[i]), xb.shape[1]))
+        check_topk_row(f[i], e, 2048, got[i], ld_canary=CANARY)
+        check_topk_layout(f[i], e, 2048, got[i])
+
+
+@pytest.mark.parametrize("cols", inputs.PREFILL_COLS)
+def test_prefill_full_size_sampled(cols):
+    """The prefill workload at full size, in the launch configuration the
+    benchmark times; rows sampled for the oracle, properties on all rows."""
+    rows, k, ld_out = inputs.PREFILL_ROWS, inputs.PREFILL_K, inputs.PREFILL_LD_OUT
+    x, ends = inputs.prefill(rows=rows, cols=cols, seed=1236, device=DEV)
+    out = torch.full((rows, ld_out), CANARY, dtype=torch.int32, device=DEV)
+    satk.topk_rows(x, k, row_ends=ends, out=out)
+    got = out.cpu().numpy()
+    sample = np.unique(np.concatenate([[0, 1, rows - 1], np.random.default_rng(cols).integers(0, rows, 40)]))
+    xs = x[sample].cpu().numpy()
+    want = np.full((len(sample), ld_out), CANARY, dtype=np.int32)
+    oracle.topk_rows(xs, k, row_ends=ends[sample].cpu().numpy(), out=want)
+    assert_rows_equal(got[sample], want, f"prefill {cols} sampled")
+    # every row: ids in range, unique, -1 free, canaries intact
+    assert np.all(got[:, k:] == CANARY)
+    e = ends.cpu().numpy()
+    assert np.all(got[:, :k] >= 0) and np.all(got[:, :k] < e[:, None])
+    srt = np.sort(got[:, :k], axis=1)
+    assert np.all(srt[:, 1:] != srt[:, :-1])
+
+
+# ------------------------------------------------------------------ pack --
+
+def test_pack_matches_oracle():
+    W, T, S, n = 4, 16, 5000, 128
+    lg, _, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=512, skew_count=50, seed=9)
+    x = lg.view(W * T, S)
+    xb = bits_of(x)
+    g = torch.Generator().manual_seed(1)
+    local = torch.randint(-3, S + 3, (W * T, n), generator=g, dtype=torch.int32)
+    local[0] = torch.arange(n)
+    ends = torch.randint(0, S + 10, (W * T,), generator=g, dtype=torch.int32)
+    xb[3, :] = 0x7FC1  # a NaN row
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+    got = satk.dcp_pack(x.to(DEV), local.to(DEV), row_ends=ends.to(DEV)).cpu().numpy()
+    want = oracle.dcp_pack(xb, local.numpy(), row_ends=ends.numpy())
+    assert_rows_equal(got, want, "pack")
+
+
+def test_pack_hand_worked_example_on_gpu():
+    from test_oracle_pins import _pack_golden_inputs
+    g, logits, idx, S = _pack_golden_inputs()
+    x = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    got = satk.dcp_pack(x, torch.from_numpy(idx).to(DEV),
+                        row_ends=torch.tensor([S], dtype=torch.int32, device=DEV)).cpu().numpy()
+    want = np.zeros(33, dtype=np.int32)
+    for e in g:
+        want[e["j"]] = e["word"]
+    want[32] = 0x22
+    assert got[0].tolist() == want.tolist()
+
+
+# ----------------------------------------------------------------- merges --
+
+@pytest.mark.parametrize("W,R,k,local", [(8, 48, 2048, 16384), (2, 20, 512, 4096),
+                                         (4, 9, 1024, 3000), (16, 6, 2048, 4096)])
+def test_pairs_merge_matches_oracle(W, R, k, local):
+    cand = inputs.pairs_merge(W=W, rows=R, k=k, local=local, seed=W * R)
+    got = satk.dcp_merge_select(cand.to(DEV), k, packed=False).cpu().numpy()
+    want = oracle.merge_pairs(cand.numpy(), k)
+    assert_rows_equal(got, want, f"pairs W={W}")
+
+
+def test_pairs_merge_ties_empties_and_short_rows():
+    W, T, n, k = 4, 6, 64, 96
+    g = torch.Generator().manual_seed(5)
+    sc = torch.tensor([1.0, 2.0, -0.0, 0.0, float("inf"), float("nan")])[
+        torch.randint(0, 6, (W, T, n), generator=g)]
+    gid = torch.randperm(W * T * n, generator=g).view(W, T, n).to(torch.int32)
+    gid[:, 1, ::3] = -1                                   # empties
+    gid[:, 2, 5:] = -1                                    # a short row
+    cand = torch.stack([sc.contiguous().view(torch.int32), gid], dim=-1).contiguous()
+    for kk in (1, 7, k, W * n, W * n + 5):
+        got = satk.dcp_merge_select(cand.to(DEV), kk, packed=False).cpu().numpy()
+        want = oracle.merge_pairs(cand.numpy(), kk)
+        assert_rows_equal(got, want, f"pairs ties k={kk}")
+
+
+def test_pairs_merge_full_size_sampled():
+    W, R, k = 8, 6710, 2048
+    cand = inputs.pairs_merge(W=W, rows=R, k=k, local=16384, seed=1236, device=DEV)
+    got = satk.dcp_merge_select(cand, k, packed=False).cpu().numpy()
+    sample = np.unique(np.concatenate([[0, R - 1], np.random.default_rng(3).integers(0, R, 30)]))
+    cs = cand[:, sample].contiguous().cpu().numpy()
+    want = oracle.merge_pairs(cs, k)
+    assert_rows_equal(got[sample], want, "pairs full size sampled")
+
+
+def _decode_gpu(lg, n, k, row_ends=None):
+    W, T, S = lg.shape
+    g = lg.to(DEV)
+    re = None if row_ends is None else row_ends.to(DEV)
+    local = satk.topk_rows(g.view(W * T, S), n, row_ends=None if re is None else re.view(-1))
+    packed = satk.dcp_pack(g.view(W * T, S), local,
+                           row_ends=None if re is None else re.view(-1)).view(W, T, n + n // 32)
+    sat = torch.zeros(T, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ids1 = satk.dcp_merge_select(packed, k, packed=True, sat_word=sat, status=status)
+    slots = (k - 1) // n
+    recv = torch.full((T * slots * (k + k // 32),), 123, dtype=torch.int32, device=DEV)
+    ids2 = ids1.clone()
+    satk.dcp_rescue_select(packed, g, sat, ids2, k, recv=recv, row_ends=re, status=status)
+    torch.cuda.synchronize()
+    return dict(local=local.cpu().numpy(), packed=packed.cpu().numpy(), ids1=ids1.cpu().numpy(),
+                sat=sat.cpu().numpy(), ids2=ids2.cpu().numpy(),
+                recv=recv.cpu().numpy().reshape(T, slots, k + k // 32),
+                status=int(status.item()))
+
+
+def _decode_oracle(lg, n, k, row_ends=None):
+    W, T, S = lg.shape
+    bits = bits_of(lg)
+    re = None if row_ends is None else row_ends.numpy()
+    local = oracle.topk_rows(bits.reshape(W * T, S), n,
+                             row_ends=None if re is None else re.reshape(-1))
+    packed = oracle.dcp_pack(bits.reshape(W * T, S), local,
+                             row_ends=None if re is None else re.reshape(-1)).reshape(
+        W, T, n + n // 32)
+    ids1, sat, st1 = oracle.merge_packed(packed, k)
+    slots = (k - 1) // n
+    recv = np.full((T, slots, k + k // 32), 123, dtype=np.int32)
+    ids2, recv, st2 = oracle.rescue(packed, k, bits, sat, ids1.copy(), row_ends=re, recv=recv)
+    return dict(local=local, packed=packed, ids1=ids1, sat=sat, ids2=ids2, recv=recv,
+                status=st1 | st2)
+
+
+def _compare_decode(got, want, what):
+    for key in ("local", "packed", "ids1", "sat", "ids2", "recv"):
+        a, b = got[key], want[key]
+        a2 = a.reshape(a.shape[0], -1) if a.ndim > 2 else a.reshape(len(a), -1)
+        b2 = b.reshape(b.shape[0], -1) if b.ndim > 2 else b.reshape(len(b), -1)
+        assert_rows_equal(a2, b2, f"{what}: {key}")
+    assert got["status"] == want["status"], f"{what}: status {got['status']} vs {want['status']}"
+
+
+def test_decode_merge_full_workload():
+    W, T, S, n, k = 8, 128, 65536, 384, 2048
+    lg, skewed, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, seed=1237, device=DEV)
+    lg = lg.cpu()
+    got = _decode_gpu(lg, n, k)
+    want = _decode_oracle(lg, n, k)
+    _compare_decode(got, want, "decode full")
+    mask = (want["sat"].astype(np.int64) & 0xFFFFFFFF) >> 16
+    assert np.array_equal(mask != 0, skewed.cpu().numpy())
+    bits = bits_of(lg)
+    for t in range(T):
+        check_decode_merge_row(got["ids2"][t], bits, t, k)
+    packed_contract(got["packed"].reshape(W * T, -1), bits.reshape(W * T, S), None, n)
+
+
+def test_decode_merge_row_ends_nan_and_small():
+    W, T, S, n, k = 4, 12, 3000, 64, 512
+    lg, _, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, skew_count=120, seed=77)
+    bits = bits_of(lg)
+    bits[2, 5, ::2] = 0xFFC3                 # half of a rank's row NaN
+    lg = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    g = torch.Generator().manual_seed(2)
+    ends = torch.randint(0, S + 50, (W, T), generator=g, dtype=torch.int32)
+    ends[0, 0] = 0
+    ends[1, 1] = 10
+    got = _decode_gpu(lg, n, k, row_ends=ends)
+    want = _decode_oracle(lg, n, k, row_ends=ends)
+    _compare_decode(got, want, "decode small")
+
+
+def test_packed_merge_out_of_contract_words():
+    """Repeated words (a NaN row's arbitrary ids on the page) and more
+    saturated ranks than slots: bit-exact status, ids and sat_word.  Row 0
+    repeats one word per rank, so the repeated key straddles the cut at
+    k = 48: fewer than k are chosen, tau16 falls to 0 and all four full
+    ranks count as saturated, more than the one rescue slot."""
+    W, T, n, k = 4, 3, 32, 48
+    words = n + n // 32
+    p = np.zeros((W, T, words), dtype=np.int32)
+    hi = np.uint32((0xBF80 << 16) | (0xFFFF - 3))
+    p[:, 0, :n] = np.array([hi] * n, dtype=np.uint32).view(np.int32)     # duplicates
+    rng = np.random.default_rng(0)
+    for r in range(W):  # every rank full and high: 4 saturated ranks, 1 slot
+        sc = rng.integers(0xC000, 0xF000, size=n).astype(np.uint32)
+        p[r, 1, :n] = ((sc << 16) | (0xFFFF - np.arange(n, dtype=np.uint32))).view(np.int32)
+    p[:, 2, :n] = np.int32(5)                                          # zero score field
+    got_sat = torch.zeros(T, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ids = satk.dcp_merge_select(torch.from_numpy(p).to(DEV), k, packed=True, sat_word=got_sat,
+                                status=st)
+    w_ids, w_sat, w_st = oracle.merge_packed(p, k)
+    assert_rows_equal(ids.cpu().numpy(), w_ids, "out of contract ids")
+    assert got_sat.cpu().numpy().tolist() == w_sat.tolist()
+    assert int(st.item()) == w_st
+
+
+# -------------------------------------------------------------- ABI edges --
+
+def test_abi_rejects_with_real_buffers():
+    x = torch.zeros((4, 100), device=DEV)
+    out = torch.zeros((4, 8), dtype=torch.int32, device=DEV)
+    L = binding.lib()
+    import ctypes
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    assert L.satk_topk_rows(p(x), 0, 4, 100, 99, None, 8, p(out), 8, None) == -1
+    assert L.satk_topk_rows(p(x), 0, 4, 100, 100, None, 9, p(out), 8, None) == -1
+    assert L.satk_topk_rows(p(x), 5, 4, 100, 100, None, 8, p(out), 8, None) == -1
+    assert L.satk_dcp_merge_select(p(out), 1, 17, 1, 32, 8, p(out), 8, None, None, None) == -1
+    assert L.satk_dcp_merge_select(p(out), 0, 1, 1, 48, 8, p(out), 8, None, None, None) == -1
+    torch.cuda.synchronize()
+    assert np.all(out.cpu().numpy() == 0)  # nothing was launched
