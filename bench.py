@@ -140,11 +140,14 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workload --
 
-def make_prefill(device):
+def make_prefill(device, widths=WIDTHS, rows=ROWS):
     data = []
-    for i, cols in enumerate(WIDTHS):
+    for cols in widths:
+        i = WIDTHS.index(cols)
         x, ends = inputs.prefill(rows=ROWS, cols=cols, seed=1236 + i, device=device)
-        out = torch.full((ROWS, LD_OUT), -7, dtype=torch.int32, device=device)
+        if rows != ROWS:  # a smaller case for profiler captures: the last rows
+            x, ends = x[-rows:].contiguous(), ends[-rows:].contiguous()
+        out = torch.full((rows, LD_OUT), -7, dtype=torch.int32, device=device)
         data.append((cols, x, ends, out))
     return data
 
@@ -184,25 +187,32 @@ def cpu_sample_rows():
 
 
 def time_oracle_prefill(host_data, nthreads=0):
-    """One bounded sample of the workload through the oracle: every
-    CPU_SAMPLE_STRIDE-th row of each width.  Returns (rows, seconds)."""
+    """One bounded sample of the workload through the oracle (the sampled
+    rows of each width).  Returns (rows, seconds)."""
     import oracle
-    sel = cpu_sample_rows()
     rows = 0
     t0 = time.perf_counter()
     for cols, x, ends in host_data:
-        oracle.topk_rows(x[sel], K, row_ends=ends[sel], nthreads=nthreads)
-        rows += len(sel)
+        oracle.topk_rows(x, K, row_ends=ends, nthreads=nthreads)
+        rows += x.shape[0]
     return rows, time.perf_counter() - t0
 
 
-def host_prefill_sample():
+def host_prefill_sample(device_data=None):
+    """The sampled rows of each width as host arrays: copied from the device
+    inputs when given (the very rows the GPU arm processes), else generated
+    with the same seeds on the best available device."""
     sel = cpu_sample_rows()
     out = []
-    for i, cols in enumerate(WIDTHS):
-        x, ends = inputs.prefill(rows=ROWS, cols=cols, seed=1236 + i, device="cpu")
-        out.append((cols, np.ascontiguousarray(x.numpy()[sel]) if False else x.numpy(),
-                    ends.numpy()))
+    if device_data is None:
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        device_data = [(cols,) + inputs.prefill(rows=ROWS, cols=cols, seed=1236 + i, device=dev)
+                       for i, cols in enumerate(WIDTHS)]
+    for item in device_data:
+        cols, x, ends = item[0], item[1], item[2]
+        idx = torch.as_tensor(sel, device=x.device)
+        out.append((cols, np.ascontiguousarray(x.index_select(0, idx).cpu().numpy()),
+                    np.ascontiguousarray(ends.index_select(0, idx).cpu().numpy())))
     return out, sel
 
 
@@ -328,7 +338,9 @@ def run_gpu(args):
     barrier(world)
     dev = torch.device("cuda", torch.cuda.current_device())
     peak, peak_kind = measured_peaks()
-    data = make_prefill(dev)
+    widths = WIDTHS if not args.only else tuple(int(c) for c in args.only.split(","))
+    rows = args.rows
+    data = make_prefill(dev, widths, rows)
     flush = inputs.flush_buffer(dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -346,7 +358,7 @@ def run_gpu(args):
 
     # ---- device-timed region: inputs resident, K steps
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in WIDTHS] for _ in range(args.steps)]
+           for _ in widths] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -360,8 +372,8 @@ def run_gpu(args):
     barrier(world)
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     per_width_ms = [statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1])
-                                    for s in range(args.steps)) for j in range(len(WIDTHS))]
-    rows_step = ROWS * len(WIDTHS)
+                                    for s in range(args.steps)) for j in range(len(widths))]
+    rows_step = rows * len(widths)
     value = rows_step * args.steps * world / (total_ms * 1e-3)
 
     # ---- end to end: pinned host inputs -> device -> ids -> host, every step
@@ -393,17 +405,18 @@ def run_gpu(args):
 
     # ---- roofline of the dominant kernel (largest share of the step)
     j = int(np.argmax(per_width_ms))
-    cols = WIDTHS[j]
-    alg = algorithmic_bytes(cols)
+    cols = widths[j]
+    alg = algorithmic_bytes(cols, rows)
     achieved = alg / (per_width_ms[j] * 1e-3) / 1e9
-    kernel_tag = f"topk_rows_stream_f32_{cols}"
+    kernel_tag = f"topk_rows_{'stream' if cols > 8192 else 'reg'}_f32_{cols}"
     traffic = recorded_traffic(kernel_tag)
-    widths = {}
-    for jj, c in enumerate(WIDTHS):
-        ab = algorithmic_bytes(c)
+    per_width = {}
+    for jj, c in enumerate(widths):
+        ab = algorithmic_bytes(c, rows)
         gbs = ab / (per_width_ms[jj] * 1e-3) / 1e9
-        widths[str(c)] = {"us": per_width_ms[jj] * 1e3, "rows_per_s": ROWS / (per_width_ms[jj] * 1e-3),
-                          "gbs": gbs, "frac": gbs / peak, "alg_bytes": ab}
+        per_width[str(c)] = {"us": per_width_ms[jj] * 1e3,
+                             "rows_per_s": rows / (per_width_ms[jj] * 1e-3),
+                             "gbs": gbs, "frac": gbs / peak, "alg_bytes": ab}
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
@@ -413,22 +426,24 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "rows_per_step": rows_step, "k": K,
                    "l2": "inputs (2.55 GB per step) larger than L2; flush buffer before stages",
                    "parallelism": f"replicas x{world} (rows independent, no collective)"},
-        "gpu_launches": len(WIDTHS) * args.steps,
+        "gpu_launches": len(widths) * args.steps,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": kernel_tag, "peak_kind": peak_kind,
                      "alg_bytes_per_launch": alg},
-        "widths": widths,
+        "widths": per_width,
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_stages:
         line["stages"] = stage_figures(dev, flush, peak)
+    if args.only or rows != ROWS:
+        line["config"]["workload"] = f"profiling subset: widths {list(widths)}, last {rows} rows"
     if rank == 0 and not args.no_cpu:
         import oracle
         oracle.build()
-        host, sel = host_prefill_sample()
+        host, sel = host_prefill_sample(data)
         rows, dt = time_oracle_prefill(host)
         line["cpu_baseline"] = {"value": rows / dt, "unit": "rows/s",
                                 "cores": oracle.default_threads(), "kind": "oracle",
@@ -450,6 +465,8 @@ def main():
     ap.add_argument("--impl", default="satk", choices=["satk", "reference"])
     ap.add_argument("--no-stages", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", default="", help="profiling aid: comma-separated widths")
+    ap.add_argument("--rows", type=int, default=ROWS, help="profiling aid: rows per width")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
