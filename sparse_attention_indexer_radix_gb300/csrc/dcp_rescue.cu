@@ -27,21 +27,20 @@
 namespace satk {
 namespace {
 
-constexpr int kPushBlock = 512;
-constexpr int kPushLkpt = 8;
+constexpr int kPushBlock = 256;
 
 __device__ __forceinline__ int nth_set_bit(uint32_t mask, int s) {
   for (int q = 0; q < s; ++q) mask &= mask - 1u;
   return __ffs(mask) - 1;
 }
 
-template <bool VECLOAD>
+template <int SUB, bool VECLOAD>
 __global__ void __launch_bounds__(kPushBlock) rescue_push_kernel(
     const uint16_t *__restrict__ logits, int64_t S, int64_t ld, int W, int64_t T, int K,
     int slots, const int32_t *__restrict__ row_ends, const int32_t *__restrict__ sat_word,
     int32_t *__restrict__ recv, int32_t *__restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  using SM = StreamSmem<kPushBlock, kPushBlock * kPushLkpt>;
+  using SM = ListSmem<kPushBlock, SUB>;
   auto &sm = *reinterpret_cast<SM *>(smem_raw);
   uint32_t *bp = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SM));
   const int64_t t = blockIdx.x / slots;
@@ -64,17 +63,32 @@ __global__ void __launch_bounds__(kPushBlock) rescue_push_kernel(
   for (int i = threadIdx.x; i < words; i += kPushBlock) bp[i] = 0u;
   zero_hist(sm.sel);
   __syncthreads();
-  topk_stream_row<uint16_t, kPushBlock, kPushLkpt, VECLOAD, true>(
+  // the rank's local top-K in the B' layout: ord16 << 16 | ~local[15:0],
+  // local[16] in the bit plane
+  topk_row<uint16_t, kPushBlock, SUB, VECLOAD>(
       logits + ((int64_t)r * T + t) * ld, static_cast<int>(end), K,
-      [&](int pos, uint32_t key, int col) {
+      [&](int pos, int i) {
         if ((unsigned)pos >= (unsigned)K) return;
-        bp[pos] = key | (0xffffu - ((uint32_t)col & 0xffffu));
-        if (((uint32_t)col >> 16) & 1u) atomicOr(bp + K + pos / 32, 1u << (pos & 31));
+        const uint32_t col = sm.val[i];
+        bp[pos] = sm.key[i] | (0xffffu - (col & 0xffffu));
+        if ((col >> 16) & 1u) atomicOr(bp + K + pos / 32, 1u << (pos & 31));
       },
       [](int) {}, sm);
   __syncthreads();
   int32_t *dst = recv + ((int64_t)t * slots + s) * words;
   for (int i = threadIdx.x; i < words; i += kPushBlock) dst[i] = static_cast<int32_t>(bp[i]);
+}
+
+template <int SUB, bool VECLOAD>
+int launch_push(const uint16_t *logits, int64_t S, int64_t ld, int W, int64_t T, int K, int slots,
+                const int32_t *row_ends, const int32_t *sat_word, int32_t *recv,
+                int32_t *status, cudaStream_t st) {
+  auto kern = rescue_push_kernel<SUB, VECLOAD>;
+  const size_t smem = sizeof(ListSmem<kPushBlock, SUB>) + sizeof(uint32_t) * (size_t)(K + K / 32);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(T * slots)), kPushBlock, smem, st>>>(
+      logits, S, ld, W, T, K, slots, row_ends, sat_word, recv, status);
+  return launch_status();
 }
 
 template <int BLOCK, int KPT>
@@ -184,21 +198,18 @@ extern "C" int satk_dcp_rescue_select(const int32_t *packed, int32_t W, int64_t 
   const cudaStream_t st = as_stream(stream);
 
   // 1. pushes of the saturated ranks
-  const size_t push_smem = sizeof(StreamSmem<kPushBlock, kPushBlock * kPushLkpt>) +
-                           sizeof(uint32_t) * (size_t)(k + k / 32);
-  const dim3 pgrid(static_cast<unsigned>(T * slots));
-  if (aligned16(logits_bf16) && (ld_logits * 2) % 16 == 0) {
-    auto kern = rescue_push_kernel<true>;
-    if (!allow_smem(kern, push_smem)) return SATK_ECUDA;
-    kern<<<pgrid, kPushBlock, push_smem, st>>>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
-                                               sat_word, recv, status);
-  } else {
-    auto kern = rescue_push_kernel<false>;
-    if (!allow_smem(kern, push_smem)) return SATK_ECUDA;
-    kern<<<pgrid, kPushBlock, push_smem, st>>>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
-                                               sat_word, recv, status);
-  }
-  int rc = launch_status();
+  const bool vec = aligned16(logits_bf16) && (ld_logits * 2) % 16 == 0;
+  int rc;
+  if (k <= 1024)
+    rc = vec ? launch_push<512, true>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+                                      sat_word, recv, status, st)
+             : launch_push<512, false>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+                                       sat_word, recv, status, st);
+  else
+    rc = vec ? launch_push<1024, true>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+                                       sat_word, recv, status, st)
+             : launch_push<1024, false>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+                                        sat_word, recv, status, st);
   if (rc != SATK_OK) return rc;
 
   // 2. the re-select over round-1 words and the pushed lists

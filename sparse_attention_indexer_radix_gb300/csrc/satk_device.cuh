@@ -141,7 +141,7 @@ __device__ __forceinline__ int block_warp_prefix(int wv, int *wtot, int *total) 
 template <int BLOCK>
 struct SelectSmem {
   uint32_t hist[2048];      // digit histogram, kept zero between passes
-  int wtot[2][BLOCK / 32];  // scan scratch (double-buffered)
+  int wtot[4][BLOCK / 32];  // scan scratch: [0] thresholds, [1]-[3] by caller
   int scal[8];              // broadcast scalars
   uint32_t red[BLOCK / 32]; // reductions
 };

@@ -1,0 +1,223 @@
+// satk_list.cuh -- candidate lists in shared memory and the exact select
+// over them.
+//
+// A row's candidates are first filtered into an ordered list that provably
+// holds the row's K best, then the K best are selected exactly on the list.
+// The list lives in per-warp segments: warp w owns entries
+// [base_w, base_w + cnt_w) of the shared arrays key[] and val[], and the
+// order of the row is (warp, entry): warp segments follow one another in
+// row order and each segment is in row order.  key is the ordered score key
+// (0 = no candidate) and val the id to emit (column, or global id).
+//
+// The select is a most-significant-digit radix select whose digits are
+// taken relative to the list's own key range: with kmin and kmax the
+// smallest and largest key, digits are cut from key - kmin over the
+// bit-length of kmax - kmin.  A list gathered above a threshold spans a
+// narrow range, so its top absolute bits are all equal; relative digits
+// spread it over the bins, which keeps the shared-memory histogram atomics
+// free of pile-ups without any warp aggregation.
+#pragma once
+
+#include "satk_device.cuh"
+
+namespace satk {
+
+template <int BLOCK, int SUB>
+struct ListSmem {
+  static constexpr int NW = BLOCK / 32;
+  static constexpr int CAP = NW * SUB;
+  SelectSmem<BLOCK> sel;
+  uint32_t key[CAP];
+  uint32_t val[CAP];
+  int cnt[NW];
+  int flag;
+};
+
+// This thread's share of the list: warp w's segment, lane-strided.  The
+// loop bound rounds the segment up to whole warps so that every lane of a
+// warp runs the same iterations (entries past the segment read as key 0).
+struct Seg {
+  int base;
+  int cnt;
+  __device__ __forceinline__ int rounds() const { return (cnt + 31) >> 5; }
+};
+
+template <int BLOCK>
+__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, SelectSmem<BLOCK> &sm) {
+  mn = __reduce_min_sync(kFull, mn);
+  mx = __reduce_max_sync(kFull, mx);
+  if (lane_id() == 0) {
+    sm.red[warp_id()] = mn;
+    sm.wtot[1][warp_id()] = static_cast<int>(mx);
+  }
+  __syncthreads();
+  uint32_t a = 0xffffffffu, b = 0u;
+#pragma unroll
+  for (int w = 0; w < BLOCK / 32; ++w) {
+    a = min(a, sm.red[w]);
+    b = max(b, static_cast<uint32_t>(sm.wtot[1][w]));
+  }
+  __syncthreads();
+  mn = a;
+  mx = b;
+}
+
+// Radix select of the K largest keys among the list entries gk(i) != 0 of
+// this thread's segment.  Outcome as Sel (see satk_device.cuh); the
+// threshold T is an absolute key.  gk may return 0 to drop an entry.
+template <int BLOCK, class GetKey>
+__device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &sm) {
+  const int lane = lane_id();
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  int n = 0;
+  for (int j = 0; j < sg.rounds(); ++j) {
+    const int i = j * 32 + lane;
+    const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
+    if (k != 0u) {
+      mn = min(mn, k);
+      mx = max(mx, k);
+      ++n;
+    }
+  }
+  // count through a scan, min/max through reductions
+  int total;
+  block_excl_scan<BLOCK>(n, sm.wtot[2], &total);
+  block_minmax<BLOCK>(mn, mx, sm);
+  Sel r;
+  r.tie = false;
+  r.take_all = false;
+  r.total = total;
+  if (total < K) {
+    r.take_all = true;
+    r.T = 1u;
+    r.need = 0;
+    return r;
+  }
+  const uint32_t span = mx - mn;
+  const int b = span == 0u ? 0 : 32 - __clz(span);
+  int need = K;
+  uint32_t prefix = 0u;
+  int pbits = 0;
+  while (pbits < b) {
+    const int width = (b - pbits) < 11 ? (b - pbits) : 11;
+    const int shift = b - pbits - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int j = 0; j < sg.rounds(); ++j) {
+      const int i = j * 32 + lane;
+      const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
+      if (k != 0u) {
+        const uint32_t rel = k - mn;
+        if (pbits == 0 || (rel >> (shift + width)) == prefix)
+          atomicAdd(sm.hist + ((rel >> shift) & dmask), 1u);
+      }
+    }
+    __syncthreads();
+    const PassOut p = find_threshold<BLOCK, 2048>(sm, need);
+    need -= p.above;
+    prefix = (prefix << width) | static_cast<uint32_t>(p.d);
+    pbits += width;
+    if (p.cnt == need) {
+      r.T = mn + (prefix << shift);
+      r.need = need;
+      return r;
+    }
+  }
+  // every key bit resolved: the K-th key is mn + prefix and `need` of the
+  // keys equal to it are still wanted (more than need share it)
+  r.T = mn + prefix;
+  r.need = need;
+  r.tie = true;
+  return r;
+}
+
+// Ordered compaction over the list segments: cls(i) = 0 skip, 1 group A,
+// 2 group B for absolute entry i; emitA/emitB(rank, i, tot) as in
+// ordered_emit.  Two barriers.
+template <int BLOCK, class Cls, class EmitA, class EmitB>
+__device__ int2 list_emit(Cls cls, const Seg &sg, EmitA emitA, EmitB emitB, SelectSmem<BLOCK> &sm) {
+  const int lane = lane_id();
+  const unsigned lt = (1u << lane) - 1u;
+  int ca = 0, cb = 0;
+  for (int j = 0; j < sg.rounds(); ++j) {
+    const int i = j * 32 + lane;
+    const int c = i < sg.cnt ? cls(sg.base + i) : 0;
+    ca += __popc(__ballot_sync(kFull, c == 1));
+    cb += __popc(__ballot_sync(kFull, c == 2));
+  }
+  int total;
+  const unsigned base =
+      (unsigned)block_warp_prefix<BLOCK>((ca << 16) | cb, sm.wtot[3], &total);
+  const int2 tot = make_int2((int)((unsigned)total >> 16), (int)((unsigned)total & 0xffffu));
+  int ra = (int)(base >> 16), rb = (int)(base & 0xffffu);
+  for (int j = 0; j < sg.rounds(); ++j) {
+    const int i = j * 32 + lane;
+    const int c = i < sg.cnt ? cls(sg.base + i) : 0;
+    const unsigned ba = __ballot_sync(kFull, c == 1);
+    const unsigned bb = __ballot_sync(kFull, c == 2);
+    if (c == 1) emitA(ra + __popc(ba & lt), sg.base + i, tot);
+    if (c == 2) emitB(rb + __popc(bb & lt), sg.base + i, tot);
+    ra += __popc(ba);
+    rb += __popc(bb);
+  }
+  __syncthreads();
+  return tot;
+}
+
+// Row top-K layout from the list: entries above the K-th key in list order,
+// then entries equal to it in list order up to K, then fill(pos) up to K.
+template <int BLOCK, int SUB, class Put, class Fill>
+__device__ void list_topk_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, Put put,
+                               Fill fill) {
+  auto gk = [&](int i) { return sm.key[i]; };
+  const Sel sel = list_select<BLOCK>(gk, sg, K, sm.sel);
+  uint32_t v;
+  if (sel.take_all) {
+    v = 0u;
+  } else if (sel.tie) {
+    v = sel.T;
+  } else {
+    uint32_t m = 0xffffffffu;
+    for (int j = 0; j < sg.rounds(); ++j) {
+      const int i = j * 32 + lane_id();
+      const uint32_t k = i < sg.cnt ? sm.key[sg.base + i] : 0u;
+      if (k >= sel.T) m = min(m, k);
+    }
+    v = block_min<BLOCK>(m, sm.sel);
+  }
+  const bool all = sel.take_all;
+  const int2 tot = list_emit<BLOCK>(
+      [&](int i) -> int {
+        const uint32_t k = sm.key[i];
+        if (k == 0u) return 0;
+        if (all) return 1;
+        return k > v ? 1 : (k == v ? 2 : 0);
+      },
+      sg, [&](int rank, int i, int2) { put(rank, i); },
+      [&](int rank, int i, int2 t) {
+        if (rank < K - t.x) put(t.x + rank, i);
+      },
+      sm.sel);
+  const int nsel = all ? max(0, min(tot.x, K)) : K;
+  for (int q = nsel + (int)threadIdx.x; q < K; q += BLOCK) fill(q);
+}
+
+// ------------------------------------------------------- thresholds ------
+
+// The float whose ordered key is the smallest key >= T among the keys a
+// dtype of KB bits can take (bf16 keys are multiples of 2**16); -inf when T
+// is at or below the key of -inf, so that a float compare x >= result
+// holds exactly for the non-NaN x with key(x) >= T.
+template <int KB>
+__device__ __forceinline__ float threshold_float(uint32_t T) {
+  if (KB == 16) T = (T > 0xffff0000u) ? 0xffff0000u : ((T + 0xffffu) & 0xffff0000u);
+  const uint32_t neg_inf_key = KB == 16 ? 0x007f0000u : 0x007fffffu;
+  if (T <= neg_inf_key) return __uint_as_float(0xff800000u);
+  // +0.0 and -0.0 compare equal as floats: a threshold at +0.0 moves to
+  // -0.0 (one key lower), keeping the compare exact
+  const uint32_t pos_zero = 0x80000000u;
+  if (T == pos_zero) T = KB == 16 ? 0x7fff0000u : 0x7fffffffu;
+  const uint32_t bits = (T & 0x80000000u) ? (T & 0x7fffffffu) : ~T;
+  return __uint_as_float(bits);
+}
+
+}  // namespace satk

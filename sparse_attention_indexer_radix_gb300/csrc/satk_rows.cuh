@@ -1,4 +1,4 @@
-// satk_rows.cuh -- exact top-K of one row, two ways.
+// satk_rows.cuh -- exact top-K of one row of fp32 or bf16 logits.
 //
 // Semantics follow [Perf][DSA] Use DeepSelect for eligible sparse-indexer
 // prefill chunks (vLLM PR #57206), Purpose and Test Plan: row i's
@@ -9,91 +9,208 @@
 // the K-th score in ascending column order, then the ids tied with it
 // (lowest columns first) up to K.
 //
-// topk_reg_row   : the whole valid row is held in registers (one 16-byte
-//                  load per VEC columns), radix select + ordered emit in
-//                  place.  One HBM read, no re-reads.
-// topk_stream_row: rows longer than the registers hold.  Pass 1 streams the
-//                  row from HBM once and builds the top-digit histogram; the
-//                  collection pass re-reads it (from L2 while the row is
-//                  resident) and compacts, in column order, every candidate
-//                  at or above the threshold digit into a shared-memory list
-//                  of at most CAP entries; the register engine then runs on
-//                  the list.  If the threshold digit holds too many
-//                  candidates for the list, further digit passes narrow it
-//                  first; at full key resolution only the first `need`
-//                  entries of the tied key are kept, so the list never
-//                  exceeds K.
+// One CTA per row, three steps:
+//  1. threshold: a strided sample of the row (4 columns per thread) is
+//     ranked and a key T0 picked so that, with a margin of about four
+//     standard deviations of the sampling error, at least K columns of the
+//     row score at or above it.  Rows no longer than the list capacity skip
+//     this and take every valid column.
+//  2. collection: the row is streamed from HBM once, each warp over its own
+//     contiguous stretch of columns; a column is kept when its score
+//     compares >= T0 as a float (one compare per element; NaN never
+//     passes).  Kept columns are ballot-compacted, in column order, into
+//     the warp's segment of the shared-memory list.
+//  3. select: the exact K-th key on the list, then the ordered emit.
+// The collection is exact, never approximate: it fails only when the list
+// is too short (T0 above the K-th key) or a warp's segment overflows, and
+// then the row is redone by the two-pass method below, which always fits:
+// a digit histogram of the whole row picks the threshold digit (narrowed by
+// more digit passes until its candidates fit the list), then an ordered
+// collection pass gathers the candidates.
 #pragma once
 
 #include <type_traits>
 
-#include "satk_device.cuh"
+#include "satk_list.cuh"
 
 namespace satk {
 
-// ---------------------------------------------------------------- in regs --
-
-template <typename T, int BLOCK, int KPT, bool VECLOAD, bool AGG, class Put, class Fill>
-__device__ __forceinline__ void topk_reg_row(const T *__restrict__ xr, int end, int K, Put put,
-                                             Fill fill, SelectSmem<BLOCK> &sm) {
-  constexpr int VEC = VECLOAD ? KeyOf<T>::kVec : 1;
-  constexpr int KB = KeyOf<T>::kBits;
-  static_assert(KPT % VEC == 0, "KPT must hold whole vectors");
-  uint32_t keys[KPT];
-  if constexpr (VECLOAD) {
-    uint4 raw[KPT / VEC];
-#pragma unroll
-    for (int g = 0; g < KPT / VEC; ++g) {
-      const int c0 = flat_pos<KPT, VEC>(g * VEC);
-      if (c0 + VEC <= end) raw[g] = ldg_stream(xr + c0);
-    }
-#pragma unroll
-    for (int g = 0; g < KPT / VEC; ++g) {
-      const int c0 = flat_pos<KPT, VEC>(g * VEC);
-      if (c0 + VEC <= end) {
-        KeyOf<T>::vec(raw[g], &keys[g * VEC]);
-      } else {
-#pragma unroll
-        for (int s = 0; s < VEC; ++s)
-          keys[g * VEC + s] = (c0 + s < end) ? KeyOf<T>::scalar(xr + c0 + s) : 0u;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < KPT; ++i) {
-      const int c = flat_pos<KPT, 1>(i);
-      keys[i] = c < end ? KeyOf<T>::scalar(xr + c) : 0u;
-    }
-  }
-  auto gk = [&](int i) { return keys[i]; };
-  const Sel sel = radix_select<BLOCK, KPT, KB, AGG>(gk, K, sm);
-  emit_topk_layout<BLOCK, KPT, VEC>(
-      gk, [&](int pos, int i) { put(pos, keys[i], flat_pos<KPT, VEC>(i)); }, fill, K, sel, sm);
+template <typename T>
+__device__ __forceinline__ float as_float(uint32_t raw) {  // one element's bits
+  if constexpr (std::is_same<T, float>::value)
+    return __uint_as_float(raw);
+  else
+    return __uint_as_float(raw << 16);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t key_of_raw(uint32_t raw) {
+  if constexpr (std::is_same<T, float>::value)
+    return key_f32(raw);
+  else
+    return key_bf16(raw);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t load_raw(const T *p) {
+  if constexpr (std::is_same<T, float>::value)
+    return __float_as_uint(__ldg(p));
+  else
+    return __ldg(reinterpret_cast<const unsigned short *>(p));
+}
+// element s of a 16-byte vector, as raw bits
+template <typename T>
+__device__ __forceinline__ uint32_t vec_raw(const uint4 &v, int s) {
+  constexpr int PER = KeyOf<T>::kVec / 4;  // elements per 32-bit word
+  const uint32_t w = s < PER ? v.x : s < 2 * PER ? v.y : s < 3 * PER ? v.z : v.w;
+  if constexpr (std::is_same<T, float>::value)
+    return w;
+  else
+    return (s & 1) ? (w >> 16) : (w & 0xffffu);
 }
 
-// ------------------------------------------------------------- streaming --
+// ------------------------------------------------------------ threshold --
 
-template <int BLOCK, int CAP>
-struct StreamSmem {
-  SelectSmem<BLOCK> sel;
-  uint32_t lkey[CAP];
-  int32_t lcol[CAP];
-};
+// Samples BLOCK*SPT columns evenly over [0, end) and returns a key T0 with
+// P(fewer than K columns of the row have key >= T0) negligible under
+// random sampling: T0 is the sample's r-th largest key, r = mu + 4 sqrt(mu)
+// + 4 with mu = K * samples / end.  Returns 1 (every valid column) when the
+// sample holds fewer than r valid keys.
+template <typename T, int BLOCK, int SPT, int SUB>
+__device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
+                                     ListSmem<BLOCK, SUB> &sm) {
+  static_assert(SPT * 32 <= SUB, "samples must fit a warp segment");
+  constexpr int S = BLOCK * SPT;
+  const int lane = lane_id(), warp = warp_id();
+  uint32_t raw[SPT];
+#pragma unroll
+  for (int q = 0; q < SPT; ++q) {
+    const int j = warp * 32 * SPT + q * 32 + lane;
+    const int pos = static_cast<int>((static_cast<int64_t>(j) * end) / S);
+    raw[q] = load_raw(xr + pos);
+  }
+#pragma unroll
+  for (int q = 0; q < SPT; ++q) sm.key[warp * SUB + q * 32 + lane] = key_of_raw<T>(raw[q]);
+  const float mu = static_cast<float>(K) * S / static_cast<float>(end);
+  int r = static_cast<int>(ceilf(mu + 4.f * sqrtf(mu) + 4.f));
+  r = r < 1 ? 1 : (r > S ? S : r);
+  __syncwarp();
+  const Seg sg{warp * SUB, 32 * SPT};
+  const Sel s = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, r, sm.sel);
+  return s.take_all ? 1u : s.T;
+}
+
+// ---------------------------------------------------- single-pass filter --
+
+// Every warp streams its own contiguous stretch of 16-byte vectors (U per
+// lane in flight) and appends the columns whose score compares >= t0f to
+// its list segment, in column order.  The < VEC ragged columns at the end
+// go to the last warp.  Returns the segment; sets sm.flag on overflow.
+template <typename T, int BLOCK, int SUB, bool VECLOAD, int U>
+__device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int end, float t0f,
+                                                ListSmem<BLOCK, SUB> &sm) {
+  constexpr int VEC = VECLOAD ? KeyOf<T>::kVec : 1;
+  constexpr int NW = BLOCK / 32;
+  const int lane = lane_id(), warp = warp_id();
+  const unsigned lt = (1u << lane) - 1u;
+  const int nvec = end / VEC;
+  const int per = (nvec + NW - 1) / NW;
+  const int v0 = min(nvec, warp * per), v1 = min(nvec, v0 + per);
+  uint32_t *lk = sm.key + warp * SUB;
+  uint32_t *lv = sm.val + warp * SUB;
+  int cnt = 0;
+  // nvals consecutive columns col0.. of this lane; p[s]: column s is kept
+  auto append = [&](const bool *p, const uint32_t *rawv, int col0) {
+    bool any = false;
+#pragma unroll
+    for (int s = 0; s < VEC; ++s) any |= p[s];
+    if (!__any_sync(kFull, any)) return;
+    unsigned b[VEC];
+    int pre = 0;
+#pragma unroll
+    for (int s = 0; s < VEC; ++s) {
+      b[s] = __ballot_sync(kFull, p[s]);
+      pre += __popc(b[s] & lt);
+    }
+#pragma unroll
+    for (int s = 0; s < VEC; ++s) {
+      if (p[s]) {
+        const int pos = cnt + pre;
+        if (pos < SUB) {
+          lk[pos] = key_of_raw<T>(rawv[s]);
+          lv[pos] = static_cast<uint32_t>(col0 + s);
+        }
+        ++pre;
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < VEC; ++s) cnt += __popc(b[s]);
+  };
+  for (int vb = v0; vb < v1; vb += 32 * U) {
+    uint4 rv[U];
+    uint32_t rs[U];
+    if constexpr (VECLOAD) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int vi = vb + u * 32 + lane;
+        if (vi < v1) rv[u] = ldg_stream(xr + static_cast<size_t>(vi) * VEC);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int vi = vb + u * 32 + lane;
+        rs[u] = vi < v1 ? load_raw(xr + vi) : 0u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = vb + u * 32 + lane;
+      const bool in = vi < v1;
+      uint32_t rawv[VEC];
+      bool p[VEC];
+#pragma unroll
+      for (int s = 0; s < VEC; ++s) {
+        if constexpr (VECLOAD)
+          rawv[s] = vec_raw<T>(rv[u], s);
+        else
+          rawv[s] = rs[u];
+        p[s] = in && as_float<T>(rawv[s]) >= t0f;
+      }
+      append(p, rawv, vi * VEC);
+    }
+  }
+  if (VECLOAD && warp == NW - 1 && nvec * VEC < end) {  // ragged columns
+    const int c = nvec * VEC + lane;
+    uint32_t rawv[VEC];
+    bool p[VEC];
+#pragma unroll
+    for (int s = 0; s < VEC; ++s) {
+      rawv[s] = 0u;
+      p[s] = false;
+    }
+    if (c < end) {
+      rawv[0] = load_raw(xr + c);
+      p[0] = as_float<T>(rawv[0]) >= t0f;
+    }
+    append(p, rawv, c);
+  }
+  if (cnt > SUB && lane == 0) sm.flag = 1;
+  return Seg{warp * SUB, min(cnt, SUB)};
+}
+
+// ------------------------------------------------------ exact (fallback) --
 
 // Visits the row [0, end) tile by tile with a warp-contiguous mapping: in a
 // tile of BLOCK*U vectors, warp w owns vectors [w*32*U, (w+1)*32*U) and
 // lane l reads vector w*32*U + u*32 + l at step u (coalesced per step).
-// body(kk, colbase) gets the lane's U*VEC keys (0 past the end) and the
-// column of kk[u*VEC] for each u via colbase[u]; every thread of the block
-// calls body the same number of times (block-uniform trip count), so body
-// may use warp collectives and barriers.  A last call with U=1 and VEC=1
-// semantics handles the < VEC ragged columns (warp 0 lanes only).
+// body(kk, col) gets the lane's U*VEC keys (0 past the end) and the column
+// of kk[u*VEC] in col[u]; every thread makes the same calls, so body may
+// use warp collectives and barriers.  A last call to tail(k, c) covers the
+// < VEC ragged columns (warp 0, one per lane).
 template <typename T, int BLOCK, int U, bool VECLOAD, class Body, class TailBody>
 __device__ __forceinline__ void for_row_tiles(const T *__restrict__ xr, int end, Body body,
                                               TailBody tail) {
   constexpr int VEC = VECLOAD ? KeyOf<T>::kVec : 1;
   const int lane = lane_id(), warp = warp_id();
-  const int nvec = end / VEC;  // whole vectors
+  const int nvec = end / VEC;
   for (int tile = 0; tile < nvec; tile += BLOCK * U) {
     uint32_t kk[U * VEC];
     int col[U];
@@ -103,7 +220,7 @@ __device__ __forceinline__ void for_row_tiles(const T *__restrict__ xr, int end,
       for (int u = 0; u < U; ++u) {
         const int vi = tile + warp * (32 * U) + u * 32 + lane;
         col[u] = vi * VEC;
-        if (vi < nvec) raw[u] = ldg_stream(xr + (size_t)vi * VEC);
+        if (vi < nvec) raw[u] = ldg_stream(xr + static_cast<size_t>(vi) * VEC);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -136,27 +253,33 @@ __device__ __forceinline__ void for_row_tiles(const T *__restrict__ xr, int end,
   }
 }
 
-template <typename T, int BLOCK, int LKPT, bool VECLOAD, bool AGG, class Put, class Fill>
-__device__ void topk_stream_row(const T *__restrict__ xr, int end, int K, Put put, Fill fill,
-                                StreamSmem<BLOCK, BLOCK * LKPT> &sm) {
+// The two-pass method: digit histogram(s) of the whole row, then an ordered
+// collection of every candidate at or above the threshold digit into the
+// list [0, CAP).  At full key resolution with a tie wider than the list,
+// only the first `need` tied columns are kept, so the list never exceeds K
+// there.  Returns this warp's share of the list.
+template <typename T, int BLOCK, int SUB, bool VECLOAD>
+__device__ Seg collect_exact(const T *__restrict__ xr, int end, int K,
+                             ListSmem<BLOCK, SUB> &sm) {
   constexpr int VEC = VECLOAD ? KeyOf<T>::kVec : 1;
-  constexpr int U = VECLOAD ? 4 : 8;
+  constexpr int U = VECLOAD ? 16 / VEC : 8;  // 16 keys per lane per tile
   constexpr int KB = KeyOf<T>::kBits;
-  constexpr int CAP = BLOCK * LKPT;
+  constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
   constexpr int NK = U * VEC;
+  constexpr int NW = BLOCK / 32;
   static_assert(BLOCK * U * VEC < 65536, "tile counts must fit 16 bits");
   SelectSmem<BLOCK> &ss = sm.sel;
   const int lane = lane_id();
   const unsigned lt = (1u << lane) - 1u;
 
-  // ---- pass 1: top-digit histogram (HBM read)
+  // ---- pass 1: top-digit histogram
   for_row_tiles<T, BLOCK, U, VECLOAD>(
       xr, end,
       [&](const uint32_t *kk, const int *) {
 #pragma unroll
-        for (int j = 0; j < NK; ++j) hist_add<AGG>(ss.hist, kk[j] >> 21, kk[j] != 0u);
+        for (int j = 0; j < NK; ++j) hist_add<true>(ss.hist, kk[j] >> 21, kk[j] != 0u);
       },
-      [&](uint32_t k, int) { hist_add<AGG>(ss.hist, k >> 21, k != 0u); });
+      [&](uint32_t k, int) { hist_add<true>(ss.hist, k >> 21, k != 0u); });
   __syncthreads();
   PassOut p = find_threshold<BLOCK, 2048>(ss, K);
 
@@ -166,20 +289,19 @@ __device__ void topk_stream_row(const T *__restrict__ xr, int end, int K, Put pu
   if (p.d < 0) {
     thr = 1u;  // fewer than K valid: every valid column
   } else {
-    uint32_t prefix = (uint32_t)p.d;
+    uint32_t prefix = static_cast<uint32_t>(p.d);
     int pbits = 11;
     int above = p.above;
     int cnt = p.cnt;
     need = K - above;
-    // ---- narrow the threshold digit until its candidates fit the list
-    while (above + cnt > CAP && pbits < KB) {
+    while (above + cnt > CAP && pbits < KB) {  // narrow the threshold digit
       const int width = (KB - pbits >= 11) ? 11 : (KB - pbits);
       const int shift = 32 - pbits - width;
       const uint32_t dmask = (1u << width) - 1u;
       const int pb = pbits;
       const uint32_t pf = prefix;
       auto visit = [&](uint32_t k) {
-        hist_add<AGG>(ss.hist, (k >> shift) & dmask, k != 0u && (k >> (32 - pb)) == pf);
+        hist_add<true>(ss.hist, (k >> shift) & dmask, k != 0u && (k >> (32 - pb)) == pf);
       };
       for_row_tiles<T, BLOCK, U, VECLOAD>(
           xr, end,
@@ -198,16 +320,16 @@ __device__ void topk_stream_row(const T *__restrict__ xr, int end, int K, Put pu
       above += p.above;
       need -= p.above;
       cnt = p.cnt;
-      prefix = (prefix << width) | (uint32_t)p.d;
+      prefix = (prefix << width) | static_cast<uint32_t>(p.d);
       pbits += width;
     }
     thr = prefix << (32 - pbits);
     limited = above + cnt > CAP;  // full resolution, tie too wide: keep `need`
   }
 
-  // ---- collection: ordered compaction of the candidates into the list
-  int runA = 0, runB = 0;  // block-uniform running counts
-  int tile_par = 0;
+  // ---- ordered collection into the list
+  int runA = 0, runB = 0;
+  int par = 0;
   auto collect = [&](const uint32_t *kk, const int *col, auto nk_tag, auto vec_tag) {
     constexpr int NKT = decltype(nk_tag)::value;
     constexpr int VT = decltype(vec_tag)::value;
@@ -215,15 +337,13 @@ __device__ void topk_stream_row(const T *__restrict__ xr, int end, int K, Put pu
 #pragma unroll
     for (int j = 0; j < NKT; ++j) {
       const uint32_t k = kk[j];
-      const bool a = limited ? (k > thr) : (k >= thr);
-      const bool b = limited && k == thr;
-      ca += __popc(__ballot_sync(kFull, a));
-      cb += __popc(__ballot_sync(kFull, b));
+      ca += __popc(__ballot_sync(kFull, limited ? (k > thr) : (k >= thr)));
+      cb += __popc(__ballot_sync(kFull, limited && k == thr));
     }
     int tot;
     const unsigned base =
-        (unsigned)block_warp_prefix<BLOCK>((ca << 16) | cb, ss.wtot[tile_par], &tot);
-    tile_par ^= 1;
+        (unsigned)block_warp_prefix<BLOCK>((ca << 16) | cb, ss.wtot[par], &tot);
+    par ^= 1;
     int ra = runA + (int)(base >> 16), rb = runB + (int)(base & 0xffffu);
 #pragma unroll
     for (int u = 0; u < NKT / VT; ++u) {
@@ -246,8 +366,8 @@ __device__ void topk_stream_row(const T *__restrict__ xr, int end, int K, Put pu
         if (a) pos = ra + pa + (limited ? min(rb + pbb, need) : 0);
         if (b && rb + pbb < need) pos = ra + pa + rb + pbb;
         if (pos >= 0 && pos < CAP) {
-          sm.lkey[pos] = k;
-          sm.lcol[pos] = col[u] + s;
+          sm.key[pos] = k;
+          sm.val[pos] = static_cast<uint32_t>(col[u] + s);
         }
         pa += a;
         pbb += b;
@@ -273,19 +393,41 @@ __device__ void topk_stream_row(const T *__restrict__ xr, int end, int K, Put pu
       });
   __syncthreads();
   const int nlist = min(CAP, runA + (limited ? min(runB, need) : 0));
+  const int chunk = (nlist + NW - 1) / NW;
+  const int b0 = min(nlist, warp_id() * chunk);
+  return Seg{b0, min(nlist, b0 + chunk) - b0};
+}
 
-  // ---- the register engine on the list (column order = list order)
-  uint32_t keys[LKPT];
-#pragma unroll
-  for (int i = 0; i < LKPT; ++i) {
-    const int f = flat_pos<LKPT, 1>(i);
-    keys[i] = f < nlist ? sm.lkey[f] : 0u;
+// ----------------------------------------------------------------- a row --
+
+// The whole row: threshold, collection (exact fallback when needed), select
+// and emit.  put(pos, i) stores list entry i at output position pos;
+// fill(pos) pads [n, K).  The histogram must be zero on entry and is zero
+// again on return.
+template <typename T, int BLOCK, int SUB, bool VECLOAD, class Put, class Fill>
+__device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill fill,
+                         ListSmem<BLOCK, SUB> &sm) {
+  constexpr int KB = KeyOf<T>::kBits;
+  constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
+  constexpr int U = VECLOAD ? (KeyOf<T>::kVec == 8 ? 4 : 8) : 8;
+  const bool all = end <= CAP;
+  float t0f;
+  if (all) {
+    t0f = __uint_as_float(0xff800000u);  // -inf: every valid column
+  } else {
+    t0f = threshold_float<KB>(sample_threshold<T, BLOCK, 4, SUB>(xr, end, K, sm));
   }
-  auto gk = [&](int i) { return keys[i]; };
-  const Sel sel = radix_select<BLOCK, LKPT, KB, AGG>(gk, K, ss);
-  emit_topk_layout<BLOCK, LKPT, 1>(
-      gk, [&](int pos, int i) { put(pos, keys[i], sm.lcol[flat_pos<LKPT, 1>(i)]); }, fill, K,
-      sel, ss);
+  if (threadIdx.x == 0) sm.flag = 0;
+  __syncthreads();  // sample keys read, flag clear
+  Seg sg = collect_filtered<T, BLOCK, SUB, VECLOAD, U>(xr, end, t0f, sm);
+  int total;
+  block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[2], &total);
+  const bool ok = sm.flag == 0 && (all || total >= K);
+  if (!ok) {  // block-uniform
+    __syncthreads();
+    sg = collect_exact<T, BLOCK, SUB, VECLOAD>(xr, end, K, sm);
+  }
+  list_topk_emit<BLOCK, SUB>(sm, sg, K, put, fill);
 }
 
 }  // namespace satk

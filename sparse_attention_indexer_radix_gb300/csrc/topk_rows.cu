@@ -3,9 +3,9 @@
 // ([Perf][DSA] Use DeepSelect for eligible sparse-indexer prefill chunks,
 // vLLM PR #57206: Purpose, Test Plan).
 //
-// One CTA per row.  Rows that fit the CTA's registers (BLOCK * KPT columns)
-// take the register path; longer rows the streaming path (see
-// satk_rows.cuh).  Both read each valid column from HBM once.
+// One CTA of 256 threads per row; the row path of satk_rows.cuh reads each
+// valid column from HBM once (sampled threshold, filtered collection into
+// a shared-memory list, exact select on the list).
 #include <climits>
 
 #include "satk_host.hpp"
@@ -14,75 +14,52 @@
 namespace satk {
 namespace {
 
+constexpr int kBlock = 256;
+
 __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, int cols) {
   if (row_ends == nullptr) return cols;
   const int e = row_ends[row];
   return e < 0 ? 0 : (e > cols ? cols : e);
 }
 
-template <typename T, int BLOCK, int KPT, bool VECLOAD, bool AGG>
-__global__ void __launch_bounds__(BLOCK) topk_rows_reg_kernel(const T *__restrict__ x, int64_t ld,
-                                                              int cols,
-                                                              const int32_t *__restrict__ row_ends,
-                                                              int K, int32_t *__restrict__ out,
-                                                              int64_t ld_out) {
-  __shared__ SelectSmem<BLOCK> sm;
-  const int64_t row = blockIdx.x;
-  const int end = row_end_of(row_ends, row, cols);
-  zero_hist(sm);
-  __syncthreads();
-  int32_t *o = out + row * ld_out;
-  topk_reg_row<T, BLOCK, KPT, VECLOAD, AGG>(
-      x + row * ld, end, K, [&](int pos, uint32_t, int col) {
-        if ((unsigned)pos < (unsigned)K) o[pos] = col;
-      },
-      [&](int pos) { o[pos] = -1; }, sm);
-}
-
-template <typename T, int BLOCK, int LKPT, bool VECLOAD, bool AGG>
-__global__ void __launch_bounds__(BLOCK) topk_rows_stream_kernel(
-    const T *__restrict__ x, int64_t ld, int cols, const int32_t *__restrict__ row_ends, int K,
-    int32_t *__restrict__ out, int64_t ld_out) {
+template <typename T, int BLOCK, int SUB, bool VECLOAD>
+__global__ void __launch_bounds__(BLOCK, 4) topk_rows_kernel(const T *__restrict__ x, int64_t ld,
+                                                          int cols,
+                                                          const int32_t *__restrict__ row_ends,
+                                                          int K, int32_t *__restrict__ out,
+                                                          int64_t ld_out) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  auto &sm = *reinterpret_cast<StreamSmem<BLOCK, BLOCK * LKPT> *>(smem_raw);
+  auto &sm = *reinterpret_cast<ListSmem<BLOCK, SUB> *>(smem_raw);
   const int64_t row = blockIdx.x;
   const int end = row_end_of(row_ends, row, cols);
   zero_hist(sm.sel);
   __syncthreads();
   int32_t *o = out + row * ld_out;
-  topk_stream_row<T, BLOCK, LKPT, VECLOAD, AGG>(
-      x + row * ld, end, K, [&](int pos, uint32_t, int col) {
-        if ((unsigned)pos < (unsigned)K) o[pos] = col;
+  topk_row<T, BLOCK, SUB, VECLOAD>(
+      x + row * ld, end, K,
+      [&](int pos, int i) {
+        if ((unsigned)pos < (unsigned)K) o[pos] = static_cast<int32_t>(sm.val[i]);
       },
       [&](int pos) { o[pos] = -1; }, sm);
 }
 
-constexpr int kBlock = 512;
-constexpr int kStreamLkpt = 8;  // list of 4096 candidates
+template <typename T, int SUB, bool VECLOAD>
+int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
+           int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_kernel<T, kBlock, SUB, VECLOAD>;
+  const size_t smem = sizeof(ListSmem<kBlock, SUB>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(rows)), kBlock, smem, st>>>(x, ld, cols, row_ends, K, out,
+                                                                ld_out);
+  return launch_status();
+}
 
+// The list holds 8 warps x SUB candidates: 4096 for K <= 1024, else 8192.
 template <typename T, bool VECLOAD>
 int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
-  constexpr int VEC = VECLOAD ? KeyOf<T>::kVec : 1;
-  const dim3 grid(static_cast<unsigned>(rows));
-  // register path: BLOCK * KPT columns, KPT a multiple of the vector width
-  constexpr int K1 = VEC > 4 ? VEC : 4;
-  if (cols <= kBlock * K1) {
-    topk_rows_reg_kernel<T, kBlock, K1, VECLOAD, true>
-        <<<grid, kBlock, 0, st>>>(x, ld, cols, row_ends, K, out, ld_out);
-  } else if (cols <= kBlock * 2 * K1) {
-    topk_rows_reg_kernel<T, kBlock, 2 * K1, VECLOAD, true>
-        <<<grid, kBlock, 0, st>>>(x, ld, cols, row_ends, K, out, ld_out);
-  } else if (cols <= kBlock * 16 && 16 % VEC == 0 && 16 > 2 * K1) {
-    topk_rows_reg_kernel<T, kBlock, 16, VECLOAD, true>
-        <<<grid, kBlock, 0, st>>>(x, ld, cols, row_ends, K, out, ld_out);
-  } else {
-    auto kern = topk_rows_stream_kernel<T, kBlock, kStreamLkpt, VECLOAD, true>;
-    const size_t smem = sizeof(StreamSmem<kBlock, kBlock * kStreamLkpt>);
-    if (!allow_smem(kern, smem)) return SATK_ECUDA;
-    kern<<<grid, kBlock, smem, st>>>(x, ld, cols, row_ends, K, out, ld_out);
-  }
-  return launch_status();
+  if (K <= 1024) return launch<T, 512, VECLOAD>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  return launch<T, 1024, VECLOAD>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
 }
 
 }  // namespace
