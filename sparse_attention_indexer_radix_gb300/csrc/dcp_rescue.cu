@@ -34,7 +34,7 @@ __device__ __forceinline__ int nth_set_bit(uint32_t mask, int s) {
   return __ffs(mask) - 1;
 }
 
-template <int SUB, bool VECLOAD>
+template <int SUB, int ALIGN>
 __global__ void __launch_bounds__(kPushBlock) rescue_push_kernel(
     const uint16_t *__restrict__ logits, int64_t S, int64_t ld, int W, int64_t T, int K,
     int slots, const int32_t *__restrict__ row_ends, const int32_t *__restrict__ sat_word,
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kPushBlock) rescue_push_kernel(
   __syncthreads();
   // the rank's local top-K in the B' layout: ord16 << 16 | ~local[15:0],
   // local[16] in the bit plane
-  topk_row<uint16_t, kPushBlock, SUB, VECLOAD>(
+  topk_row<uint16_t, kPushBlock, SUB, ALIGN>(
       logits + ((int64_t)r * T + t) * ld, static_cast<int>(end), K,
       [&](int pos, int i) {
         if ((unsigned)pos >= (unsigned)K) return;
@@ -79,11 +79,11 @@ __global__ void __launch_bounds__(kPushBlock) rescue_push_kernel(
   for (int i = threadIdx.x; i < words; i += kPushBlock) dst[i] = static_cast<int32_t>(bp[i]);
 }
 
-template <int SUB, bool VECLOAD>
+template <int SUB, int ALIGN>
 int launch_push(const uint16_t *logits, int64_t S, int64_t ld, int W, int64_t T, int K, int slots,
                 const int32_t *row_ends, const int32_t *sat_word, int32_t *recv,
                 int32_t *status, cudaStream_t st) {
-  auto kern = rescue_push_kernel<SUB, VECLOAD>;
+  auto kern = rescue_push_kernel<SUB, ALIGN>;
   const size_t smem = sizeof(ListSmem<kPushBlock, SUB>) + sizeof(uint32_t) * (size_t)(K + K / 32);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   kern<<<dim3(static_cast<unsigned>(T * slots)), kPushBlock, smem, st>>>(
@@ -201,14 +201,14 @@ extern "C" int satk_dcp_rescue_select(const int32_t *packed, int32_t W, int64_t 
   const bool vec = aligned16(logits_bf16) && (ld_logits * 2) % 16 == 0;
   int rc;
   if (k <= 1024)
-    rc = vec ? launch_push<512, true>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+    rc = vec ? launch_push<512, 16>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
                                       sat_word, recv, status, st)
-             : launch_push<512, false>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+             : launch_push<512, 0>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
                                        sat_word, recv, status, st);
   else
-    rc = vec ? launch_push<1024, true>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+    rc = vec ? launch_push<1024, 16>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
                                        sat_word, recv, status, st)
-             : launch_push<1024, false>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
+             : launch_push<1024, 0>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
                                         sat_word, recv, status, st);
   if (rc != SATK_OK) return rc;
 

@@ -178,35 +178,49 @@ struct PassOut {
 // Scans the NB-bin histogram from the top digit down and finds the digit d
 // with above(d) < need <= above(d) + hist[d].  Zeroes every bin it reads,
 // so the histogram is clean for the next pass.  Ends with a barrier.
+//
+// Bins are read in groups of 32, one per lane in descending order (no bank
+// conflicts), warp w taking groups [w*GPW, (w+1)*GPW); group sums come from
+// a warp reduction, warp offsets from one block prefix, and only the warp
+// holding the crossing scans its group lane by lane.
 template <int BLOCK, int NB>
 __device__ __forceinline__ PassOut find_threshold(SelectSmem<BLOCK> &sm, int need) {
-  constexpr int BPT = NB >= BLOCK ? NB / BLOCK : 1;
-  constexpr int NT = NB / BPT;
-  const int t = threadIdx.x;
-  uint32_t c[BPT];
-  int s = 0;
+  static_assert(NB % 32 == 0, "bins come in groups of 32");
+  constexpr int NW = BLOCK / 32;
+  constexpr int NG = NB / 32;
+  constexpr int GPW = (NG + NW - 1) / NW;
+  const int lane = lane_id(), warp = warp_id();
+  uint32_t c[GPW];
+  int gs[GPW];
+  int wsum = 0;
 #pragma unroll
-  for (int b = 0; b < BPT; ++b) {
-    c[b] = 0;
-    if (t < NT) {
-      const int bin = NB - 1 - (t * BPT + b);
-      c[b] = sm.hist[bin];
+  for (int q = 0; q < GPW; ++q) {
+    const int g = warp * GPW + q;
+    c[q] = 0u;
+    if (g < NG) {
+      const int bin = NB - 1 - (g * 32 + lane);
+      c[q] = sm.hist[bin];
       sm.hist[bin] = 0u;
-      s += (int)c[b];
     }
+    gs[q] = static_cast<int>(__reduce_add_sync(kFull, c[q]));
+    wsum += gs[q];
   }
   int total;
-  const int excl = block_excl_scan<BLOCK>(s, sm.wtot[0], &total);
-  if (t < NT && s > 0 && excl < need && excl + s >= need) {
-    int cum = excl;
+  const int wbase = block_warp_prefix<BLOCK>(wsum, sm.wtot[0], &total);
+  if (total >= need && wbase < need && wbase + wsum >= need) {  // warp-uniform
+    int cum = wbase;
 #pragma unroll
-    for (int b = 0; b < BPT; ++b) {
-      if (cum < need && cum + (int)c[b] >= need) {
-        sm.scal[0] = NB - 1 - (t * BPT + b);
-        sm.scal[1] = cum;
-        sm.scal[2] = (int)c[b];
+    for (int q = 0; q < GPW; ++q) {
+      if (cum < need && cum + gs[q] >= need) {  // warp-uniform
+        const int incl = warp_incl_scan(static_cast<int>(c[q]));
+        const int before = cum + incl - static_cast<int>(c[q]);
+        if (before < need && before + static_cast<int>(c[q]) >= need) {
+          sm.scal[0] = NB - 1 - ((warp * GPW + q) * 32 + lane);
+          sm.scal[1] = before;
+          sm.scal[2] = static_cast<int>(c[q]);
+        }
       }
-      cum += (int)c[b];
+      cum += gs[q];
     }
   }
   __syncthreads();

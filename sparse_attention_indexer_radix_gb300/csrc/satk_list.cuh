@@ -65,8 +65,11 @@ __device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, SelectS
 // Radix select of the K largest keys among the list entries gk(i) != 0 of
 // this thread's segment.  Outcome as Sel (see satk_device.cuh); the
 // threshold T is an absolute key.  gk may return 0 to drop an entry.
+// With max_passes, the digit passes stop early and T is the start of the
+// threshold digit (at least K keys are >= T).
 template <int BLOCK, class GetKey>
-__device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &sm) {
+__device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &sm,
+                           int max_passes = 8) {
   const int lane = lane_id();
   uint32_t mn = 0xffffffffu, mx = 0u;
   int n = 0;
@@ -116,7 +119,7 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
     need -= p.above;
     prefix = (prefix << width) | static_cast<uint32_t>(p.d);
     pbits += width;
-    if (p.cnt == need) {
+    if (p.cnt == need || --max_passes == 0) {
       r.T = mn + (prefix << shift);
       r.need = need;
       return r;

@@ -29,6 +29,8 @@
 // collection pass gathers the candidates.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include <type_traits>
 
 #include "satk_list.cuh"
@@ -94,106 +96,173 @@ __device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
   r = r < 1 ? 1 : (r > S ? S : r);
   __syncwarp();
   const Seg sg{warp * SUB, 32 * SPT};
-  const Sel s = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, r, sm.sel);
+  const Sel s = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, r, sm.sel, 2);
   return s.take_all ? 1u : s.T;
 }
 
 // ---------------------------------------------------- single-pass filter --
 
-// Every warp streams its own contiguous stretch of 16-byte vectors (U per
-// lane in flight) and appends the columns whose score compares >= t0f to
-// its list segment, in column order.  The < VEC ragged columns at the end
-// go to the last warp.  Returns the segment; sets sm.flag on overflow.
-template <typename T, int BLOCK, int SUB, bool VECLOAD, int U>
-__device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int end, float t0f,
-                                                ListSmem<BLOCK, SUB> &sm) {
-  constexpr int VEC = VECLOAD ? KeyOf<T>::kVec : 1;
-  constexpr int NW = BLOCK / 32;
-  const int lane = lane_id(), warp = warp_id();
-  const unsigned lt = (1u << lane) - 1u;
-  const int nvec = end / VEC;
-  const int per = (nvec + NW - 1) / NW;
-  const int v0 = min(nvec, warp * per), v1 = min(nvec, v0 + per);
-  uint32_t *lk = sm.key + warp * SUB;
-  uint32_t *lv = sm.val + warp * SUB;
-  int cnt = 0;
-  // nvals consecutive columns col0.. of this lane; p[s]: column s is kept
-  auto append = [&](const bool *p, const uint32_t *rawv, int col0) {
-    bool any = false;
-#pragma unroll
-    for (int s = 0; s < VEC; ++s) any |= p[s];
-    if (!__any_sync(kFull, any)) return;
-    unsigned b[VEC];
-    int pre = 0;
-#pragma unroll
-    for (int s = 0; s < VEC; ++s) {
-      b[s] = __ballot_sync(kFull, p[s]);
-      pre += __popc(b[s] & lt);
-    }
-#pragma unroll
-    for (int s = 0; s < VEC; ++s) {
-      if (p[s]) {
-        const int pos = cnt + pre;
-        if (pos < SUB) {
-          lk[pos] = key_of_raw<T>(rawv[s]);
-          lv[pos] = static_cast<uint32_t>(col0 + s);
-        }
-        ++pre;
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < VEC; ++s) cnt += __popc(b[s]);
-  };
-  for (int vb = v0; vb < v1; vb += 32 * U) {
-    uint4 rv[U];
-    uint32_t rs[U];
-    if constexpr (VECLOAD) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int vi = vb + u * 32 + lane;
-        if (vi < v1) rv[u] = ldg_stream(xr + static_cast<size_t>(vi) * VEC);
-      }
+// 8 consecutive elements of one lane: loads and the kept-column mask (bit s
+// set when element s compares >= the threshold; NaN never does).
+// ALIGN 32: one 32-byte load (fp32, rows 32-byte aligned); 16: two 16-byte
+// loads (fp32) or one (bf16); 0: scalar loads.
+template <typename T, int ALIGN>
+struct Group8;
+
+template <int ALIGN>
+struct Group8<float, ALIGN> {
+  uint32_t w[8];
+  __device__ __forceinline__ void load(const float *p) {
+    if constexpr (ALIGN == 32) {
+      asm volatile(
+          "ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+          : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+            "=r"(w[7])
+          : "l"(p));
+    } else if constexpr (ALIGN == 16) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
+      const uint4 b = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     } else {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int vi = vb + u * 32 + lane;
-        rs[u] = vi < v1 ? load_raw(xr + vi) : 0u;
-      }
+      for (int s = 0; s < 8; ++s) w[s] = __float_as_uint(__ldg(p + s));
+    }
+  }
+  __device__ __forceinline__ uint32_t mask(float t) const {
+    uint32_t m = 0;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) m |= (__uint_as_float(w[s]) >= t ? 1u : 0u) << s;
+    return m;
+  }
+};
+
+template <int ALIGN>
+struct Group8<uint16_t, ALIGN> {
+  uint32_t w[4];  // two bf16 per word, element 2j in the low half
+  __device__ __forceinline__ void load(const uint16_t *p) {
+    if constexpr (ALIGN != 0) {
+      const uint4 a = ldg_stream(p);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    } else {
+      const unsigned short *q = reinterpret_cast<const unsigned short *>(p);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = static_cast<uint32_t>(__ldg(q + 2 * j)) |
+               (static_cast<uint32_t>(__ldg(q + 2 * j + 1)) << 16);
+    }
+  }
+  __device__ __forceinline__ uint32_t mask(__nv_bfloat162 t2) const {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t h = __hge2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]), t2);
+      m |= ((h & 1u) | ((h >> 15) & 2u)) << (2 * j);
+    }
+    return m;
+  }
+};
+
+template <typename T>
+struct ThresholdOf;
+template <>
+struct ThresholdOf<float> {
+  float t;
+  __device__ __forceinline__ explicit ThresholdOf(float f) : t(f) {}
+  __device__ __forceinline__ float arg() const { return t; }
+};
+template <>
+struct ThresholdOf<uint16_t> {
+  __nv_bfloat162 t2;
+  __device__ __forceinline__ explicit ThresholdOf(float f) {
+    // f is a bf16 value, or has only low-half bits below one (negative
+    // thresholds carry 0xffff there): round toward -inf to the bf16 grid,
+    // which admits exactly the same bf16 inputs
+    uint32_t b = __float_as_uint(f) >> 16;
+    const __nv_bfloat16 h = *reinterpret_cast<const __nv_bfloat16 *>(&b);
+    t2 = __halves2bfloat162(h, h);
+  }
+  __device__ __forceinline__ __nv_bfloat162 arg() const { return t2; }
+};
+
+// Every warp streams its own contiguous stretch of 8-element groups (one
+// group per lane, U per lane in flight) and records the columns whose score
+// compares >= the threshold in its list segment (val only; keys are filled
+// in afterwards), in column order.  Per-lane counts of each batch go
+// through one packed warp prefix scan.  The < 8 ragged columns at the end
+// go to the last warp.  Returns the segment; sets sm.flag on overflow.
+template <typename T, int BLOCK, int SUB, int ALIGN, int U>
+__device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int end, float t0f,
+                                                ListSmem<BLOCK, SUB> &sm) {
+  static_assert(U % 2 == 0, "counts are packed two per word");
+  constexpr int NW = BLOCK / 32;
+  const int lane = lane_id(), warp = warp_id();
+  const int ngroups = end / 8;
+  const int per = (ngroups + NW - 1) / NW;
+  const int g0 = min(ngroups, warp * per), g1 = min(ngroups, g0 + per);
+  uint32_t *lv = sm.val + warp * SUB;
+  const ThresholdOf<T> thr(t0f);
+  int cnt = 0;
+  for (int gb = g0; gb < g1; gb += 32 * U) {
+    Group8<T, ALIGN> grp[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int gi = gb + u * 32 + lane;
+      if (gi < g1) grp[u].load(xr + static_cast<size_t>(gi) * 8);
+    }
+    uint32_t m[U];
+    uint32_t pk[U / 2];
+#pragma unroll
+    for (int j = 0; j < U / 2; ++j) pk[j] = 0u;
+    uint32_t any = 0u;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int gi = gb + u * 32 + lane;
+      m[u] = gi < g1 ? grp[u].mask(thr.arg()) : 0u;
+      pk[u >> 1] |= static_cast<uint32_t>(__popc(m[u])) << (16 * (u & 1));
+      any |= m[u];
+    }
+    if (!__any_sync(kFull, any != 0u)) continue;
+    uint32_t incl[U / 2], tot[U / 2];
+#pragma unroll
+    for (int j = 0; j < U / 2; ++j) {
+      incl[j] = static_cast<uint32_t>(warp_incl_scan(static_cast<int>(pk[j])));
+      tot[j] = __shfl_sync(kFull, incl[j], 31);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int vi = vb + u * 32 + lane;
-      const bool in = vi < v1;
-      uint32_t rawv[VEC];
-      bool p[VEC];
-#pragma unroll
-      for (int s = 0; s < VEC; ++s) {
-        if constexpr (VECLOAD)
-          rawv[s] = vec_raw<T>(rv[u], s);
-        else
-          rawv[s] = rs[u];
-        p[s] = in && as_float<T>(rawv[s]) >= t0f;
+      const uint32_t lc = static_cast<uint32_t>(__popc(m[u]));
+      int pos = cnt + static_cast<int>(((incl[u >> 1] >> (16 * (u & 1))) & 0xffffu) - lc);
+      uint32_t mm = m[u];
+      const int c0 = (gb + u * 32 + lane) * 8;
+      while (mm != 0u) {
+        const int s = __ffs(mm) - 1;
+        mm &= mm - 1u;
+        if (pos < SUB) lv[pos] = static_cast<uint32_t>(c0 + s);
+        ++pos;
       }
-      append(p, rawv, vi * VEC);
+      cnt += static_cast<int>((tot[u >> 1] >> (16 * (u & 1))) & 0xffffu);
     }
   }
-  if (VECLOAD && warp == NW - 1 && nvec * VEC < end) {  // ragged columns
-    const int c = nvec * VEC + lane;
-    uint32_t rawv[VEC];
-    bool p[VEC];
-#pragma unroll
-    for (int s = 0; s < VEC; ++s) {
-      rawv[s] = 0u;
-      p[s] = false;
-    }
-    if (c < end) {
-      rawv[0] = load_raw(xr + c);
-      p[0] = as_float<T>(rawv[0]) >= t0f;
-    }
-    append(p, rawv, c);
+  if (warp == NW - 1 && ngroups * 8 < end) {  // ragged columns
+    const int c = ngroups * 8 + lane;
+    const bool keep = c < end && as_float<T>(load_raw(xr + c)) >= t0f;
+    const unsigned b = __ballot_sync(kFull, keep);
+    const int pos = cnt + __popc(b & ((1u << lane) - 1u));
+    if (keep && pos < SUB) lv[pos] = static_cast<uint32_t>(c);
+    cnt += __popc(b);
   }
   if (cnt > SUB && lane == 0) sm.flag = 1;
   return Seg{warp * SUB, min(cnt, SUB)};
+}
+
+// Keys of the recorded columns, read back (from L2: the row was just
+// streamed) into the warp's own segment.
+template <typename T, int BLOCK, int SUB>
+__device__ __forceinline__ void gather_keys(const T *__restrict__ xr, const Seg &sg,
+                                            ListSmem<BLOCK, SUB> &sm) {
+  for (int i = lane_id(); i < sg.cnt; i += 32)
+    sm.key[sg.base + i] = key_of_raw<T>(load_raw(xr + sm.val[sg.base + i]));
 }
 
 // ------------------------------------------------------ exact (fallback) --
@@ -404,12 +473,12 @@ __device__ Seg collect_exact(const T *__restrict__ xr, int end, int K,
 // and emit.  put(pos, i) stores list entry i at output position pos;
 // fill(pos) pads [n, K).  The histogram must be zero on entry and is zero
 // again on return.
-template <typename T, int BLOCK, int SUB, bool VECLOAD, class Put, class Fill>
+template <typename T, int BLOCK, int SUB, int ALIGN, class Put, class Fill>
 __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill fill,
                          ListSmem<BLOCK, SUB> &sm) {
   constexpr int KB = KeyOf<T>::kBits;
   constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
-  constexpr int U = VECLOAD ? (KeyOf<T>::kVec == 8 ? 4 : 8) : 8;
+  constexpr bool VECLOAD = ALIGN != 0;
   const bool all = end <= CAP;
   float t0f;
   if (all) {
@@ -419,11 +488,14 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   }
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear
-  Seg sg = collect_filtered<T, BLOCK, SUB, VECLOAD, U>(xr, end, t0f, sm);
+  Seg sg = collect_filtered<T, BLOCK, SUB, ALIGN, 4>(xr, end, t0f, sm);
   int total;
   block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[2], &total);
   const bool ok = sm.flag == 0 && (all || total >= K);
-  if (!ok) {  // block-uniform
+  if (ok) {  // block-uniform
+    gather_keys<T, BLOCK, SUB>(xr, sg, sm);
+    __syncwarp();
+  } else {
     __syncthreads();
     sg = collect_exact<T, BLOCK, SUB, VECLOAD>(xr, end, K, sm);
   }

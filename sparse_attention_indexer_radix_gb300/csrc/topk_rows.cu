@@ -22,7 +22,7 @@ __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, 
   return e < 0 ? 0 : (e > cols ? cols : e);
 }
 
-template <typename T, int BLOCK, int SUB, bool VECLOAD>
+template <typename T, int BLOCK, int SUB, int ALIGN>
 __global__ void __launch_bounds__(BLOCK, 4) topk_rows_kernel(const T *__restrict__ x, int64_t ld,
                                                           int cols,
                                                           const int32_t *__restrict__ row_ends,
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(BLOCK, 4) topk_rows_kernel(const T *__restrict
   zero_hist(sm.sel);
   __syncthreads();
   int32_t *o = out + row * ld_out;
-  topk_row<T, BLOCK, SUB, VECLOAD>(
+  topk_row<T, BLOCK, SUB, ALIGN>(
       x + row * ld, end, K,
       [&](int pos, int i) {
         if ((unsigned)pos < (unsigned)K) o[pos] = static_cast<int32_t>(sm.val[i]);
@@ -43,10 +43,10 @@ __global__ void __launch_bounds__(BLOCK, 4) topk_rows_kernel(const T *__restrict
       [&](int pos) { o[pos] = -1; }, sm);
 }
 
-template <typename T, int SUB, bool VECLOAD>
+template <typename T, int SUB, int ALIGN>
 int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
            int32_t *out, int64_t ld_out, cudaStream_t st) {
-  auto kern = topk_rows_kernel<T, kBlock, SUB, VECLOAD>;
+  auto kern = topk_rows_kernel<T, kBlock, SUB, ALIGN>;
   const size_t smem = sizeof(ListSmem<kBlock, SUB>);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   kern<<<dim3(static_cast<unsigned>(rows)), kBlock, smem, st>>>(x, ld, cols, row_ends, K, out,
@@ -55,11 +55,19 @@ int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_en
 }
 
 // The list holds 8 warps x SUB candidates: 4096 for K <= 1024, else 8192.
-template <typename T, bool VECLOAD>
+template <typename T, int ALIGN>
 int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
-  if (K <= 1024) return launch<T, 512, VECLOAD>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
-  return launch<T, 1024, VECLOAD>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (K <= 1024) return launch<T, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  return launch<T, 1024, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+}
+
+// Widest load every row start allows: 32 or 16 bytes, else element loads.
+inline int row_alignment(const void *x, int64_t ld_bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(x);
+  if ((a & 31u) == 0 && ld_bytes % 32 == 0) return 32;
+  if ((a & 15u) == 0 && ld_bytes % 16 == 0) return 16;
+  return 0;
 }
 
 }  // namespace
@@ -78,12 +86,17 @@ extern "C" int satk_topk_rows(const void *logits, int dtype, int64_t rows, int64
   const int c = static_cast<int>(cols);
   if (dtype == SATK_F32) {
     const float *x = static_cast<const float *>(logits);
-    if (aligned16(x) && (ld_logits * 4) % 16 == 0)
-      return launch_rows<float, true>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
-    return launch_rows<float, false>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+    switch (row_alignment(x, ld_logits * 4)) {
+      case 32:
+        return launch_rows<float, 32>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+      case 16:
+        return launch_rows<float, 16>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+      default:
+        return launch_rows<float, 0>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+    }
   }
   const uint16_t *x = static_cast<const uint16_t *>(logits);
-  if (aligned16(x) && (ld_logits * 2) % 16 == 0)
-    return launch_rows<uint16_t, true>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
-  return launch_rows<uint16_t, false>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+  if (row_alignment(x, ld_logits * 2) != 0)
+    return launch_rows<uint16_t, 16>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+  return launch_rows<uint16_t, 0>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
 }
