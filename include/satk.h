@@ -120,7 +120,7 @@ int satk_dcp_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
  *          int32 global id); an entry with id < 0 or a NaN score is empty.
  *          SATK_PACKED_BF16: int32 [W, T, n + n/32] B' rows; global id
  *          local * W + r for rank r, 0 words empty.
- *          Both contiguous.
+ *          Both contiguous; the pairs buffer 16-byte aligned.
  * W, n   : ranks and candidates per rank; W * n <=
  *          SATK_MERGE_MAX_CANDIDATES; packed needs W <= 16 and n % 32 == 0;
  *          pairs needs n % 32 == 0.
@@ -136,9 +136,10 @@ int satk_dcp_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
  *          bits is cleared and SATK_STATUS_SLOTS_EXCEEDED raised
  *          [P2 DCPTopkSelectKernel docstring].
  * Errors : SATK_EINVAL for NULL cand/ids_out, W < 1, T < 0, n < 1, k < 1,
- *          ld_out < k, an unknown format, a shape rule above, or a non-NULL
- *          sat_word with the pairs format; SATK_EUNSUPPORTED when W * n
- *          exceeds SATK_MERGE_MAX_CANDIDATES.
+ *          ld_out < k, an unknown format, a shape rule above, a pairs
+ *          buffer not 16-byte aligned, or a non-NULL sat_word with the
+ *          pairs format; SATK_EUNSUPPORTED when W * n exceeds
+ *          SATK_MERGE_MAX_CANDIDATES.
  */
 int satk_dcp_merge_select(const void *cand, int format, int32_t W, int64_t T,
                           int32_t n, int32_t k, int32_t *ids_out,

@@ -14,6 +14,7 @@
 #include <climits>
 
 #include "satk_host.hpp"
+#include "satk_list.cuh"
 #include "satk_merge.cuh"
 
 namespace satk {
@@ -156,6 +157,246 @@ __global__ void __launch_bounds__(BLOCK) merge_select_kernel(
   if (bits != 0 && status != nullptr && threadIdx.x == 0) atomicOr(status, bits);
 }
 
+// ----------------------------------------------------- pairs, in place --
+//
+// The (score, global id) pairs of row t: flat candidate f = r * n + j sits
+// at pair ((r * T + t) * n + j) of the rank-major buffer.  As for a row of
+// logits: a sampled threshold, one filtered pass that records flat indices
+// in per-warp list segments (each warp over its own stretch of the flat
+// range, walked in runs that stay inside one rank), then the select on the
+// list -- by score, and by global id among candidates tied with the K-th
+// score.  A pair with id < 0 or a NaN score is empty.
+
+__device__ __forceinline__ uint32_t pair_key(int2 p) {
+  return p.y >= 0 ? key_f32(static_cast<uint32_t>(p.x)) : 0u;
+}
+
+// 4 consecutive pairs of one lane (32 bytes): kept mask, bit s for pair s.
+template <int ALIGN>
+__device__ __forceinline__ uint32_t pairs4_mask(const int2 *p, float t) {
+  uint32_t w[8];
+  if constexpr (ALIGN == 32) {
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+          "=r"(w[7])
+        : "l"(p));
+  } else {
+    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+  uint32_t m = 0u;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const bool keep = __uint_as_float(w[2 * s]) >= t && static_cast<int32_t>(w[2 * s + 1]) >= 0;
+    m |= (keep ? 1u : 0u) << s;
+  }
+  return m;
+}
+
+template <int BLOCK, int SUB, int ALIGN>
+__global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
+    const int2 *__restrict__ cand, int W, int64_t T, int n, int K, int32_t *__restrict__ ids,
+    int64_t ld_out, int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  using SM = ListSmem<BLOCK, SUB>;
+  auto &sm = *reinterpret_cast<SM *>(smem_raw);
+  constexpr int NW = BLOCK / 32;
+  constexpr int CAP = SM::CAP;
+  constexpr int SPT = 4;
+  constexpr int U = 4;
+  const int64_t t = blockIdx.x;
+  const int lane = lane_id(), warp = warp_id();
+  const int total = W * n;
+  const int gpr = n / 4;  // 4-pair groups per rank
+  auto at = [&](int f) {  // pair of flat candidate f
+    const int r = f / n;
+    return cand + ((static_cast<int64_t>(r) * T + t) * n + (f - r * n));
+  };
+  zero_hist(sm.sel);
+  if (threadIdx.x == 0) sm.flag = 0;
+  __syncthreads();
+
+  // ---- threshold
+  const bool all = total <= CAP;
+  float t0f = __uint_as_float(0xff800000u);
+  if (!all) {
+    constexpr int S = BLOCK * SPT;
+#pragma unroll
+    for (int q = 0; q < SPT; ++q) {
+      const int j = warp * 32 * SPT + q * 32 + lane;
+      const int f = static_cast<int>((static_cast<int64_t>(j) * total) / S);
+      sm.key[warp * SUB + q * 32 + lane] = pair_key(__ldg(at(f)));
+    }
+    const float mu = static_cast<float>(K) * S / static_cast<float>(total);
+    int r = static_cast<int>(ceilf(mu + 4.f * sqrtf(mu) + 4.f));
+    r = r < 1 ? 1 : (r > S ? S : r);
+    __syncwarp();
+    const Sel sl = list_select<BLOCK>([&](int i) { return sm.key[i]; },
+                                      Seg{warp * SUB, 32 * SPT}, r, sm.sel, 2);
+    t0f = threshold_float<32>(sl.take_all ? 1u : sl.T);
+    __syncthreads();
+  }
+
+  // ---- filtered pass: flat indices of the kept pairs, in flat order
+  const int ngroups = total / 4;
+  const int per = (ngroups + NW - 1) / NW;
+  const int g0 = min(ngroups, warp * per), g1 = min(ngroups, g0 + per);
+  uint32_t *lv = sm.val + warp * SUB;
+  int cnt = 0;
+  for (int gr = g0; gr < g1;) {  // runs inside one rank (warp-uniform)
+    const int r = gr / gpr;
+    const int rend = min(g1, (r + 1) * gpr);
+    const int2 *base = cand + (static_cast<int64_t>(r) * T + t) * n - static_cast<int64_t>(r) * n;
+    for (int gb = gr; gb < rend; gb += 32 * U) {
+      uint32_t m[U];
+      uint32_t any = 0u;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int gi = gb + u * 32 + lane;
+        m[u] = gi < rend ? pairs4_mask<ALIGN>(base + static_cast<int64_t>(gi) * 4, t0f) : 0u;
+        any |= m[u];
+      }
+      if (!__any_sync(kFull, any != 0u)) continue;
+      uint32_t pk = 0u;
+#pragma unroll
+      for (int u = 0; u < U; ++u) pk |= static_cast<uint32_t>(__popc(m[u])) << (8 * u);
+      const uint32_t incl = static_cast<uint32_t>(warp_incl_scan(static_cast<int>(pk)));
+      const uint32_t tot = __shfl_sync(kFull, incl, 31);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t lc = static_cast<uint32_t>(__popc(m[u]));
+        int pos = cnt + static_cast<int>(((incl >> (8 * u)) & 0xffu) - lc);
+        uint32_t mm = m[u];
+        const int f0 = (gb + u * 32 + lane) * 4;
+        while (mm != 0u) {
+          const int s = __ffs(mm) - 1;
+          mm &= mm - 1u;
+          if (pos < SUB) lv[pos] = static_cast<uint32_t>(f0 + s);
+          ++pos;
+        }
+        cnt += static_cast<int>((tot >> (8 * u)) & 0xffu);
+      }
+    }
+    gr = rend;
+  }
+  if (cnt > SUB && lane == 0) sm.flag = 1;
+  Seg sg{warp * SUB, min(cnt, SUB)};
+  int listed;
+  block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[2], &listed);
+  const bool ok = sm.flag == 0 && (all || listed >= K);
+  if (!ok) {  // block-uniform: record every non-empty pair (two list passes
+              // cannot hold more than CAP, so take the exact digit path)
+    __syncthreads();
+    // exact: histogram of the top digit over all pairs, then collect keys
+    // at or above the threshold digit, narrowing while it would overflow
+    uint32_t prefix = 0u;
+    int pbits = 0, need = K, above = 0;
+    bool take_all = false;
+    while (true) {
+      const int width = pbits == 0 ? 11 : min(11, 32 - pbits);
+      const int shift = 32 - pbits - width;
+      for (int f = threadIdx.x; f < total; f += BLOCK) {
+        const uint32_t k = pair_key(__ldg(at(f)));
+        if (k != 0u && (pbits == 0 || (k >> (32 - pbits)) == prefix))
+          atomicAdd(sm.sel.hist + ((k >> shift) & ((1u << width) - 1u)), 1u);
+      }
+      __syncthreads();
+      const PassOut p = find_threshold<BLOCK, 2048>(sm.sel, need);
+      if (p.d < 0) {
+        take_all = pbits == 0;
+        break;
+      }
+      above += p.above;
+      need -= p.above;
+      prefix = (prefix << width) | static_cast<uint32_t>(p.d);
+      pbits += width;
+      if (above + p.cnt <= CAP || pbits == 32) break;
+    }
+    const uint32_t thr = take_all ? 1u : (prefix << (32 - pbits));
+    // ordered collection (flat order) of keys >= thr; at full resolution a
+    // tie wider than the list keeps the first `need` tied pairs
+    const bool limited = !take_all && pbits == 32;
+    int runA = 0, runB = 0, par = 0;
+    for (int f0 = 0; f0 < total; f0 += BLOCK) {
+      const int f = f0 + threadIdx.x;
+      const uint32_t k = f < total ? pair_key(__ldg(at(f))) : 0u;
+      const bool a = limited ? k > thr : k >= thr;
+      const bool b = limited && k == thr;
+      const unsigned ba = __ballot_sync(kFull, a), bb = __ballot_sync(kFull, b);
+      int tot2;
+      const unsigned wb = (unsigned)block_warp_prefix<BLOCK>((__popc(ba) << 16) | __popc(bb),
+                                                            sm.sel.wtot[par], &tot2);
+      par ^= 1;
+      const int pa = runA + (int)(wb >> 16) + __popc(ba & ((1u << lane) - 1u));
+      const int pb = runB + (int)(wb & 0xffffu) + __popc(bb & ((1u << lane) - 1u));
+      int pos = -1;
+      if (a) pos = pa + (limited ? min(pb, need) : 0);
+      if (b && pb < need) pos = pa + pb;
+      if (pos >= 0 && pos < CAP) sm.val[pos] = static_cast<uint32_t>(f);
+      runA += (int)((unsigned)tot2 >> 16);
+      runB += (int)((unsigned)tot2 & 0xffffu);
+    }
+    __syncthreads();
+    const int nlist = min(CAP, runA + (limited ? min(runB, need) : 0));
+    const int chunk = (nlist + NW - 1) / NW;
+    const int b0 = min(nlist, warp * chunk);
+    sg = Seg{b0, min(nlist, b0 + chunk) - b0};
+  }
+  // keys and global ids of the listed pairs
+  for (int i = lane; i < sg.cnt; i += 32) {
+    const int2 pr = __ldg(at(static_cast<int>(sm.val[sg.base + i])));
+    sm.key[sg.base + i] = pair_key(pr);
+    sm.val[sg.base + i] = static_cast<uint32_t>(pr.y);
+  }
+  __syncwarp();
+
+  // ---- select: by score, then by global id among ties with the K-th
+  const Sel s1 = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, K, sm.sel);
+  uint32_t t2 = 0u;
+  bool use2 = false, tie2 = false;
+  if (!s1.take_all && s1.tie) {
+    const Sel s2 = list_select<BLOCK>(
+        [&](int i) { return sm.key[i] == s1.T ? 0xffffffffu - sm.val[i] : 0u; }, sg, s1.need,
+        sm.sel);
+    use2 = true;
+    t2 = s2.T;
+    tie2 = s2.tie;
+  }
+  int32_t *out = ids + t * ld_out;
+  const int2 tot = list_emit<BLOCK>(
+      [&](int i) -> int {
+        const uint32_t k = sm.key[i];
+        if (k == 0u) return 0;
+        if (s1.take_all) return 1;
+        if (!use2) return k >= s1.T ? 1 : 0;
+        if (k != s1.T) return k > s1.T ? 1 : 0;
+        const uint32_t k2 = 0xffffffffu - sm.val[i];
+        return (tie2 ? k2 > t2 : k2 >= t2) ? 1 : 0;
+      },
+      sg,
+      [&](int rank, int i, int2) {
+        if ((unsigned)rank < (unsigned)K) out[rank] = static_cast<int32_t>(sm.val[i]);
+      },
+      [](int, int, int2) {}, sm.sel);
+  for (int q = max(0, tot.x) + (int)threadIdx.x; q < K; q += BLOCK) out[q] = -1;
+  if (tie2 && status != nullptr && threadIdx.x == 0) atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
+}
+
+template <int SUB, int ALIGN>
+int launch_pairs(const int32_t *cand, int W, int64_t T, int n, int K, int32_t *ids,
+                 int64_t ld_out, int32_t *status, cudaStream_t st) {
+  constexpr int BLOCK = 256;
+  auto kern = pairs_merge_kernel<BLOCK, SUB, ALIGN>;
+  const size_t smem = sizeof(ListSmem<BLOCK, SUB>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(T)), BLOCK, smem, st>>>(reinterpret_cast<const int2 *>(cand),
+                                                            W, T, n, K, ids, ld_out, status);
+  return launch_status();
+}
+
 template <int BLOCK, int KPT, bool PACKED>
 int launch_merge(const int32_t *cand, int W, int64_t T, int n, int K, int32_t *ids,
                  int64_t ld_out, int32_t *sat_word, int32_t *status, cudaStream_t st) {
@@ -209,7 +450,7 @@ extern "C" int satk_dcp_merge_select(const void *cand, int format, int32_t W, in
   if (format == SATK_PACKED_BF16) {
     if (W > 16) return SATK_EINVAL;
   } else if (format == SATK_PAIRS_F32) {
-    if (sat_word != nullptr || (reinterpret_cast<uintptr_t>(cand) & 7u) != 0) return SATK_EINVAL;
+    if (sat_word != nullptr || (reinterpret_cast<uintptr_t>(cand) & 15u) != 0) return SATK_EINVAL;
   } else {
     return SATK_EINVAL;
   }
@@ -219,5 +460,11 @@ extern "C" int satk_dcp_merge_select(const void *cand, int format, int32_t W, in
   const cudaStream_t st = as_stream(stream);
   if (format == SATK_PACKED_BF16)
     return dispatch_merge<true>(c, W, T, n, k, ids_out, ld_out, sat_word, status, st);
-  return dispatch_merge<false>(c, W, T, n, k, ids_out, ld_out, nullptr, status, st);
+  // pairs: the list holds 8 warps x SUB candidates
+  const bool a32 = (reinterpret_cast<uintptr_t>(cand) & 31u) == 0;
+  if (k <= 1024)
+    return a32 ? launch_pairs<512, 32>(c, W, T, n, k, ids_out, ld_out, status, st)
+               : launch_pairs<512, 16>(c, W, T, n, k, ids_out, ld_out, status, st);
+  return a32 ? launch_pairs<1024, 32>(c, W, T, n, k, ids_out, ld_out, status, st)
+             : launch_pairs<1024, 16>(c, W, T, n, k, ids_out, ld_out, status, st);
 }

@@ -14,7 +14,12 @@
 namespace satk {
 namespace {
 
+// 256 threads per row; rows of at most 16384 columns with K <= 512 take
+// 128 (more rows resident per SM, shorter barriers: short rows are bound by
+// the per-row select, not by the stream).
 constexpr int kBlock = 256;
+constexpr int kShortBlock = 128;
+constexpr int kShortCols = 16384;
 
 __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, int cols) {
   if (row_ends == nullptr) return cols;
@@ -23,7 +28,7 @@ __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, 
 }
 
 template <typename T, int BLOCK, int SUB, int ALIGN>
-__global__ void __launch_bounds__(BLOCK, 4) topk_rows_kernel(const T *__restrict__ x, int64_t ld,
+__global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) topk_rows_kernel(const T *__restrict__ x, int64_t ld,
                                                           int cols,
                                                           const int32_t *__restrict__ row_ends,
                                                           int K, int32_t *__restrict__ out,
@@ -43,23 +48,26 @@ __global__ void __launch_bounds__(BLOCK, 4) topk_rows_kernel(const T *__restrict
       [&](int pos) { o[pos] = -1; }, sm);
 }
 
-template <typename T, int SUB, int ALIGN>
+template <typename T, int BLOCK, int SUB, int ALIGN>
 int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
            int32_t *out, int64_t ld_out, cudaStream_t st) {
-  auto kern = topk_rows_kernel<T, kBlock, SUB, ALIGN>;
-  const size_t smem = sizeof(ListSmem<kBlock, SUB>);
+  auto kern = topk_rows_kernel<T, BLOCK, SUB, ALIGN>;
+  const size_t smem = sizeof(ListSmem<BLOCK, SUB>);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
-  kern<<<dim3(static_cast<unsigned>(rows)), kBlock, smem, st>>>(x, ld, cols, row_ends, K, out,
-                                                                ld_out);
+  kern<<<dim3(static_cast<unsigned>(rows)), BLOCK, smem, st>>>(x, ld, cols, row_ends, K, out,
+                                                               ld_out);
   return launch_status();
 }
 
-// The list holds 8 warps x SUB candidates: 4096 for K <= 1024, else 8192.
+// The list holds (BLOCK/32) warps x SUB candidates.
 template <typename T, int ALIGN>
 int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
-  if (K <= 1024) return launch<T, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
-  return launch<T, 1024, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (cols <= kShortCols && K <= 512)
+    return launch<T, kShortBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (K <= 1024)
+    return launch<T, kBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  return launch<T, kBlock, 1024, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
 }
 
 // Widest load every row start allows: 32 or 16 bytes, else element loads.
