@@ -224,10 +224,11 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   float t0f = __uint_as_float(0xff800000u);
   if (!all) {
     constexpr int S = BLOCK * SPT;
+    constexpr int NRUNS = S / 32;  // runs of 32 consecutive candidates
 #pragma unroll
     for (int q = 0; q < SPT; ++q) {
-      const int j = warp * 32 * SPT + q * 32 + lane;
-      const int f = static_cast<int>((static_cast<int64_t>(j) * total) / S);
+      const int run = warp * SPT + q;
+      const int f = (static_cast<int>((static_cast<int64_t>(run) * total) / NRUNS) & ~31) + lane;
       sm.key[warp * SUB + q * 32 + lane] = pair_key(__ldg(at(f)));
     }
     const float mu = static_cast<float>(K) * S / static_cast<float>(total);

@@ -71,23 +71,27 @@ __device__ __forceinline__ uint32_t vec_raw(const uint4 &v, int s) {
 
 // ------------------------------------------------------------ threshold --
 
-// Samples BLOCK*SPT columns evenly over [0, end) and returns a key T0 with
-// P(fewer than K columns of the row have key >= T0) negligible under
-// random sampling: T0 is the sample's r-th largest key, r = mu + 4 sqrt(mu)
-// + 4 with mu = K * samples / end.  Returns 1 (every valid column) when the
-// sample holds fewer than r valid keys.
+// Samples BLOCK*SPT columns of the row -- BLOCK*SPT/32 runs of 32
+// consecutive columns spread evenly over [0, end), one coalesced load per
+// warp and run, so the sample touches few memory sectors -- and returns a
+// key T0 with P(fewer than K columns of the row have key >= T0) negligible
+// under random sampling: T0 is the sample's r-th largest key,
+// r = mu + 4 sqrt(mu) + 4 with mu = K * samples / end.  Returns 1 (every
+// valid column) when the sample holds fewer than r valid keys.  Needs
+// end >= 32 * BLOCK * SPT / 32.
 template <typename T, int BLOCK, int SPT, int SUB>
 __device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
                                      ListSmem<BLOCK, SUB> &sm) {
   static_assert(SPT * 32 <= SUB, "samples must fit a warp segment");
   constexpr int S = BLOCK * SPT;
   const int lane = lane_id(), warp = warp_id();
+  constexpr int NRUNS = S / 32;
   uint32_t raw[SPT];
 #pragma unroll
   for (int q = 0; q < SPT; ++q) {
-    const int j = warp * 32 * SPT + q * 32 + lane;
-    const int pos = static_cast<int>((static_cast<int64_t>(j) * end) / S);
-    raw[q] = load_raw(xr + pos);
+    const int run = warp * SPT + q;
+    const int start = static_cast<int>((static_cast<int64_t>(run) * end) / NRUNS) & ~31;
+    raw[q] = load_raw(xr + start + lane);
   }
 #pragma unroll
   for (int q = 0; q < SPT; ++q) sm.key[warp * SUB + q * 32 + lane] = key_of_raw<T>(raw[q]);
@@ -112,6 +116,13 @@ struct Group8;
 template <int ALIGN>
 struct Group8<float, ALIGN> {
   uint32_t w[8];
+  // raw bits of element s (s not a compile-time constant: a select tree)
+  __device__ __forceinline__ uint32_t raw(int s) const {
+    const uint32_t a0 = (s & 1) ? w[1] : w[0], a1 = (s & 1) ? w[3] : w[2];
+    const uint32_t a2 = (s & 1) ? w[5] : w[4], a3 = (s & 1) ? w[7] : w[6];
+    const uint32_t b0 = (s & 2) ? a1 : a0, b1 = (s & 2) ? a3 : a2;
+    return (s & 4) ? b1 : b0;
+  }
   __device__ __forceinline__ void load(const float *p) {
     if constexpr (ALIGN == 32) {
       asm volatile(
@@ -140,6 +151,11 @@ struct Group8<float, ALIGN> {
 template <int ALIGN>
 struct Group8<uint16_t, ALIGN> {
   uint32_t w[4];  // two bf16 per word, element 2j in the low half
+  __device__ __forceinline__ uint32_t raw(int s) const {
+    const uint32_t a0 = (s & 2) ? w[1] : w[0], a1 = (s & 2) ? w[3] : w[2];
+    const uint32_t b = (s & 4) ? a1 : a0;
+    return (s & 1) ? (b >> 16) : (b & 0xffffu);
+  }
   __device__ __forceinline__ void load(const uint16_t *p) {
     if constexpr (ALIGN != 0) {
       const uint4 a = ldg_stream(p);
@@ -187,8 +203,8 @@ struct ThresholdOf<uint16_t> {
 
 // Every warp streams its own contiguous stretch of 8-element groups (one
 // group per lane, U per lane in flight) and records the columns whose score
-// compares >= the threshold in its list segment (val only; keys are filled
-// in afterwards), in column order.  Per-lane counts of each batch go
+// compares >= the threshold, with their keys, in its list segment, in
+// column order.  Per-lane counts of each batch go
 // through one packed warp prefix scan.  The < 8 ragged columns at the end
 // go to the last warp.  Returns the segment; sets sm.flag on overflow.
 template <typename T, int BLOCK, int SUB, int ALIGN, int U>
@@ -200,6 +216,7 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
   const int ngroups = end / 8;
   const int per = (ngroups + NW - 1) / NW;
   const int g0 = min(ngroups, warp * per), g1 = min(ngroups, g0 + per);
+  uint32_t *lk = sm.key + warp * SUB;
   uint32_t *lv = sm.val + warp * SUB;
   const ThresholdOf<T> thr(t0f);
   int cnt = 0;
@@ -238,7 +255,10 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
       while (mm != 0u) {
         const int s = __ffs(mm) - 1;
         mm &= mm - 1u;
-        if (pos < SUB) lv[pos] = static_cast<uint32_t>(c0 + s);
+        if (pos < SUB) {
+          lk[pos] = key_of_raw<T>(grp[u].raw(s));
+          lv[pos] = static_cast<uint32_t>(c0 + s);
+        }
         ++pos;
       }
       cnt += static_cast<int>((tot[u >> 1] >> (16 * (u & 1))) & 0xffffu);
@@ -246,23 +266,18 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
   }
   if (warp == NW - 1 && ngroups * 8 < end) {  // ragged columns
     const int c = ngroups * 8 + lane;
-    const bool keep = c < end && as_float<T>(load_raw(xr + c)) >= t0f;
+    const uint32_t rw = c < end ? load_raw(xr + c) : 0u;
+    const bool keep = c < end && as_float<T>(rw) >= t0f;
     const unsigned b = __ballot_sync(kFull, keep);
     const int pos = cnt + __popc(b & ((1u << lane) - 1u));
-    if (keep && pos < SUB) lv[pos] = static_cast<uint32_t>(c);
+    if (keep && pos < SUB) {
+      lk[pos] = key_of_raw<T>(rw);
+      lv[pos] = static_cast<uint32_t>(c);
+    }
     cnt += __popc(b);
   }
   if (cnt > SUB && lane == 0) sm.flag = 1;
   return Seg{warp * SUB, min(cnt, SUB)};
-}
-
-// Keys of the recorded columns, read back (from L2: the row was just
-// streamed) into the warp's own segment.
-template <typename T, int BLOCK, int SUB>
-__device__ __forceinline__ void gather_keys(const T *__restrict__ xr, const Seg &sg,
-                                            ListSmem<BLOCK, SUB> &sm) {
-  for (int i = lane_id(); i < sg.cnt; i += 32)
-    sm.key[sg.base + i] = key_of_raw<T>(load_raw(xr + sm.val[sg.base + i]));
 }
 
 // ------------------------------------------------------ exact (fallback) --
@@ -331,7 +346,7 @@ template <typename T, int BLOCK, int SUB, bool VECLOAD>
 __device__ Seg collect_exact(const T *__restrict__ xr, int end, int K,
                              ListSmem<BLOCK, SUB> &sm) {
   constexpr int VEC = VECLOAD ? KeyOf<T>::kVec : 1;
-  constexpr int U = VECLOAD ? 16 / VEC : 8;  // 16 keys per lane per tile
+  constexpr int U = VECLOAD ? 8 / VEC : 8;  // 8 keys per lane per tile
   constexpr int KB = KeyOf<T>::kBits;
   constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
   constexpr int NK = U * VEC;
@@ -492,10 +507,7 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   int total;
   block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[2], &total);
   const bool ok = sm.flag == 0 && (all || total >= K);
-  if (ok) {  // block-uniform
-    gather_keys<T, BLOCK, SUB>(xr, sg, sm);
-    __syncwarp();
-  } else {
+  if (!ok) {  // block-uniform
     __syncthreads();
     sg = collect_exact<T, BLOCK, SUB, VECLOAD>(xr, end, K, sm);
   }
