@@ -184,6 +184,41 @@ int satk_dcp_rescue_select(const int32_t *packed, int32_t W, int64_t T,
  * [P2 DCPTopkRescueWorkspace].  0 for invalid arguments. */
 size_t satk_rescue_recv_words(int64_t T, int32_t n, int32_t k);
 
+/* Scratch words available to satk_dcp_rescue_select_noalloc (8 MiB). */
+#define SATK_RESCUE_NOALLOC_MAX_WORDS (2 * 1024 * 1024)
+
+/*
+ * satk_dcp_rescue_select_noalloc -- satk_dcp_rescue_select without the
+ * `recv` argument, for callers that cannot allocate device memory (code
+ * that only receives pointers to its inputs and outputs, or runs where
+ * cudaMalloc may not be called).  The pages have no counterpart: it is a
+ * convenience of this library.
+ *
+ * The pushed lists go to a fixed array inside the library's own device
+ * memory, SATK_RESCUE_NOALLOC_MAX_WORDS int32 words on every GPU that loads
+ * the library, kept until the process exits.  Nothing is allocated and no
+ * allocating routine is called.  All other arguments, results, status bits
+ * and errors are those of satk_dcp_rescue_select; in addition a call whose
+ * satk_rescue_recv_words(T, n, k) exceeds SATK_RESCUE_NOALLOC_MAX_WORDS is
+ * rejected with SATK_EUNSUPPORTED before anything is launched.
+ *
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *   that first call before any stream capture.  A failed look-up returns
+ *   SATK_ECUDA.
+ * - Every call on a device uses the same array and leaves its contents
+ *   behind.  Nothing in it needs to start at zero: each slot a call reads
+ *   is written by that same call first.  Calls that can run at the same
+ *   time on the GPU (different streams without ordering) race on it.
+ */
+int satk_dcp_rescue_select_noalloc(const int32_t *packed, int32_t W, int64_t T,
+                                   int32_t n, int32_t k,
+                                   const uint16_t *logits_bf16, int64_t S,
+                                   int64_t ld_logits, const int32_t *row_ends,
+                                   const int32_t *sat_word, int32_t *ids_out,
+                                   int64_t ld_out, int32_t *status,
+                                   satk_stream_t stream);
+
 /* A static, human-readable string for an SATK_* return code. */
 const char *satk_status_string(int rc);
 
