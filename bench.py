@@ -232,8 +232,22 @@ def timed_calls(fn, reps, flush):
     return statistics.median(times)
 
 
-def stage_figures(dev, flush, peak):
+STAGES = ("pairs", "decode", "adversarial")
+
+
+def stage_figures(dev, flush, peak, which=STAGES):
     import sparse_attention_indexer_radix_gb300 as satk
+    st = {}
+    if "pairs" in which:
+        st.update(_stage_pairs(dev, flush, peak, satk))
+    if "decode" in which:
+        st.update(_stage_decode(dev, flush, peak, satk))
+    if "adversarial" in which:
+        st.update(_stage_adversarial(dev, flush, peak, satk))
+    return st
+
+
+def _stage_pairs(dev, flush, peak, satk):
     st = {}
     # rank-major pairs merge: W=8, 6710 rows, top-2048 of 8 x 2048 candidates
     W, R, k = 8, 6710, 2048
@@ -247,7 +261,11 @@ def stage_figures(dev, flush, peak):
     st["pairs_merge_W8_R6710_K2048"] = {
         "us": ms * 1e3, "rows_per_s": R / (ms * 1e-3), "gbs": nbytes / (ms * 1e-3) / 1e9,
         "frac": nbytes / (ms * 1e-3) / 1e9 / peak, "alg_bytes": nbytes}
-    del cand, ids
+    return st
+
+
+def _stage_decode(dev, flush, peak, satk):
+    st = {}
     # one-round decode merge: W=8, 128 rows, S=65536 bf16, N=384, K=2048
     W, T, S, n, k = 8, 128, 65536, 384, 2048
     lg, _, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, seed=1237, device=dev)
@@ -277,7 +295,11 @@ def stage_figures(dev, flush, peak):
     dec["local_topN_frac"] = dec["local_topN_gbs"] / peak
     dec["saturated_rows"] = int(((sat >> 16) != 0).sum().item())
     st["decode_merge_W8_T128_S65536_N384_K2048"] = dec
-    del lg, flat, local, packed, recv
+    return st
+
+
+def _stage_adversarial(dev, flush, peak, satk):
+    st = {}
     # adversarial bf16 top-K: 256 x 131072, 64 levels, K=2048
     x, ends, _ = inputs.adversarial(seed=1239, device=dev)
     out = torch.empty((256, 2048 + 64), dtype=torch.int32, device=dev)
@@ -408,7 +430,7 @@ def run_gpu(args):
     cols = widths[j]
     alg = algorithmic_bytes(cols, rows)
     achieved = alg / (per_width_ms[j] * 1e-3) / 1e9
-    kernel_tag = f"topk_rows_{'stream' if cols > 8192 else 'reg'}_f32_{cols}"
+    kernel_tag = f"topk_rows_kernel_f32_{cols}"
     traffic = recorded_traffic(kernel_tag)
     per_width = {}
     for jj, c in enumerate(widths):
@@ -467,11 +489,22 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default="", help="profiling aid: comma-separated widths")
     ap.add_argument("--rows", type=int, default=ROWS, help="profiling aid: rows per width")
+    ap.add_argument("--stage-only", default="",
+                    help="profiling aid: run only these stages (comma-separated: "
+                         + ",".join(STAGES) + ") and print their figures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.stage_only:
+        from sparse_attention_indexer_radix_gb300 import build as satk_build
+        satk_build.build()
+        dev = torch.device("cuda", 0)
+        peak, _ = measured_peaks()
+        which = tuple(args.stage_only.split(","))
+        print(json.dumps({"stages": stage_figures(dev, inputs.flush_buffer(dev), peak, which)}))
+        return 0
     return run_gpu(args)
 
 
