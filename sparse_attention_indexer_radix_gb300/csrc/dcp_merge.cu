@@ -171,10 +171,34 @@ __device__ __forceinline__ uint32_t pair_key(int2 p) {
   return p.y >= 0 ? key_f32(static_cast<uint32_t>(p.x)) : 0u;
 }
 
-// 4 consecutive pairs of one lane (32 bytes): kept mask, bit s for pair s.
-template <int ALIGN>
-__device__ __forceinline__ uint32_t pairs4_mask(const int2 *p, float t) {
+// 4 consecutive pairs of one lane (32 bytes): w[2s] score bits, w[2s+1] gid.
+struct Pairs4 {
   uint32_t w[8];
+  template <int ALIGN>
+  __device__ __forceinline__ void load(const int2 *p);
+  // kept mask: bit s set when pair s is non-empty and scores >= t
+  __device__ __forceinline__ uint32_t mask(float t) const {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const bool keep = __uint_as_float(w[2 * s]) >= t && static_cast<int32_t>(w[2 * s + 1]) >= 0;
+      m |= (keep ? 1u : 0u) << s;
+    }
+    return m;
+  }
+  // pair s (s not a compile-time constant: select trees)
+  __device__ __forceinline__ uint32_t score(int s) const {
+    const uint32_t a = (s & 1) ? w[2] : w[0], b = (s & 1) ? w[6] : w[4];
+    return (s & 2) ? b : a;
+  }
+  __device__ __forceinline__ uint32_t gid(int s) const {
+    const uint32_t a = (s & 1) ? w[3] : w[1], b = (s & 1) ? w[7] : w[5];
+    return (s & 2) ? b : a;
+  }
+};
+
+template <int ALIGN>
+__device__ __forceinline__ void Pairs4::load(const int2 *p) {
   if constexpr (ALIGN == 32) {
     asm volatile(
         "ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -187,13 +211,6 @@ __device__ __forceinline__ uint32_t pairs4_mask(const int2 *p, float t) {
     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
     w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
   }
-  uint32_t m = 0u;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const bool keep = __uint_as_float(w[2 * s]) >= t && static_cast<int32_t>(w[2 * s + 1]) >= 0;
-    m |= (keep ? 1u : 0u) << s;
-  }
-  return m;
 }
 
 template <int BLOCK, int SUB, int ALIGN>
@@ -241,10 +258,11 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
     __syncthreads();
   }
 
-  // ---- filtered pass: flat indices of the kept pairs, in flat order
+  // ---- filtered pass: keys and global ids of the kept pairs, flat order
   const int ngroups = total / 4;
   const int per = (ngroups + NW - 1) / NW;
   const int g0 = min(ngroups, warp * per), g1 = min(ngroups, g0 + per);
+  uint32_t *lk = sm.key + warp * SUB;
   uint32_t *lv = sm.val + warp * SUB;
   int cnt = 0;
   for (int gr = g0; gr < g1;) {  // runs inside one rank (warp-uniform)
@@ -252,12 +270,18 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
     const int rend = min(g1, (r + 1) * gpr);
     const int2 *base = cand + (static_cast<int64_t>(r) * T + t) * n - static_cast<int64_t>(r) * n;
     for (int gb = gr; gb < rend; gb += 32 * U) {
+      Pairs4 grp[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int gi = gb + u * 32 + lane;
+        if (gi < rend) grp[u].template load<ALIGN>(base + static_cast<int64_t>(gi) * 4);
+      }
       uint32_t m[U];
       uint32_t any = 0u;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int gi = gb + u * 32 + lane;
-        m[u] = gi < rend ? pairs4_mask<ALIGN>(base + static_cast<int64_t>(gi) * 4, t0f) : 0u;
+        m[u] = gi < rend ? grp[u].mask(t0f) : 0u;
         any |= m[u];
       }
       if (!__any_sync(kFull, any != 0u)) continue;
@@ -271,11 +295,13 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
         const uint32_t lc = static_cast<uint32_t>(__popc(m[u]));
         int pos = cnt + static_cast<int>(((incl >> (8 * u)) & 0xffu) - lc);
         uint32_t mm = m[u];
-        const int f0 = (gb + u * 32 + lane) * 4;
         while (mm != 0u) {
           const int s = __ffs(mm) - 1;
           mm &= mm - 1u;
-          if (pos < SUB) lv[pos] = static_cast<uint32_t>(f0 + s);
+          if (pos < SUB) {
+            lk[pos] = key_f32(grp[u].score(s));
+            lv[pos] = grp[u].gid(s);
+          }
           ++pos;
         }
         cnt += static_cast<int>((tot >> (8 * u)) & 0xffu);
@@ -336,7 +362,10 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
       int pos = -1;
       if (a) pos = pa + (limited ? min(pb, need) : 0);
       if (b && pb < need) pos = pa + pb;
-      if (pos >= 0 && pos < CAP) sm.val[pos] = static_cast<uint32_t>(f);
+      if (pos >= 0 && pos < CAP) {
+        sm.key[pos] = k;
+        sm.val[pos] = static_cast<uint32_t>(__ldg(at(f)).y);
+      }
       runA += (int)((unsigned)tot2 >> 16);
       runB += (int)((unsigned)tot2 & 0xffffu);
     }
@@ -345,12 +374,6 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
     const int chunk = (nlist + NW - 1) / NW;
     const int b0 = min(nlist, warp * chunk);
     sg = Seg{b0, min(nlist, b0 + chunk) - b0};
-  }
-  // keys and global ids of the listed pairs
-  for (int i = lane; i < sg.cnt; i += 32) {
-    const int2 pr = __ldg(at(static_cast<int>(sm.val[sg.base + i])));
-    sm.key[sg.base + i] = pair_key(pr);
-    sm.val[sg.base + i] = static_cast<uint32_t>(pr.y);
   }
   __syncwarp();
 
@@ -461,9 +484,9 @@ extern "C" int satk_dcp_merge_select(const void *cand, int format, int32_t W, in
   const cudaStream_t st = as_stream(stream);
   if (format == SATK_PACKED_BF16)
     return dispatch_merge<true>(c, W, T, n, k, ids_out, ld_out, sat_word, status, st);
-  // pairs: the list holds 8 warps x SUB candidates
+  // pairs: the list holds 8 warps x SUB candidates (4096 up to K = 2048)
   const bool a32 = (reinterpret_cast<uintptr_t>(cand) & 31u) == 0;
-  if (k <= 1024)
+  if (k <= 2048)
     return a32 ? launch_pairs<512, 32>(c, W, T, n, k, ids_out, ld_out, status, st)
                : launch_pairs<512, 16>(c, W, T, n, k, ids_out, ld_out, status, st);
   return a32 ? launch_pairs<1024, 32>(c, W, T, n, k, ids_out, ld_out, status, st)
