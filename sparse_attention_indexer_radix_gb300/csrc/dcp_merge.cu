@@ -186,15 +186,6 @@ struct Pairs4 {
     }
     return m;
   }
-  // pair s (s not a compile-time constant: select trees)
-  __device__ __forceinline__ uint32_t score(int s) const {
-    const uint32_t a = (s & 1) ? w[2] : w[0], b = (s & 1) ? w[6] : w[4];
-    return (s & 2) ? b : a;
-  }
-  __device__ __forceinline__ uint32_t gid(int s) const {
-    const uint32_t a = (s & 1) ? w[3] : w[1], b = (s & 1) ? w[7] : w[5];
-    return (s & 2) ? b : a;
-  }
 };
 
 template <int ALIGN>
@@ -253,7 +244,7 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
     r = r < 1 ? 1 : (r > S ? S : r);
     __syncwarp();
     const Sel sl = list_select<BLOCK>([&](int i) { return sm.key[i]; },
-                                      Seg{warp * SUB, 32 * SPT}, r, sm.sel, 2);
+                                      Seg{warp * SUB, 32 * SPT}, r, sm.sel, 3);
     t0f = threshold_float<32>(sl.take_all ? 1u : sl.T);
     __syncthreads();
   }
@@ -293,16 +284,19 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t lc = static_cast<uint32_t>(__popc(m[u]));
-        int pos = cnt + static_cast<int>(((incl >> (8 * u)) & 0xffu) - lc);
-        uint32_t mm = m[u];
-        while (mm != 0u) {
-          const int s = __ffs(mm) - 1;
-          mm &= mm - 1u;
-          if (pos < SUB) {
-            lk[pos] = key_f32(grp[u].score(s));
-            lv[pos] = grp[u].gid(s);
+        // a quarter or more of the pairs pass: four fixed steps with the
+        // pair index known at compile time beat a loop over the set bits
+        const int pos0 = cnt + static_cast<int>(((incl >> (8 * u)) & 0xffu) - lc);
+        const uint32_t mm = m[u];
+        if (mm != 0u) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const int pos = pos0 + __popc(mm & ((1u << s) - 1u));
+            if (((mm >> s) & 1u) && pos < SUB) {
+              lk[pos] = key_f32(grp[u].w[2 * s]);
+              lv[pos] = grp[u].w[2 * s + 1];
+            }
           }
-          ++pos;
         }
         cnt += static_cast<int>((tot >> (8 * u)) & 0xffu);
       }
@@ -311,8 +305,8 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   }
   if (cnt > SUB && lane == 0) sm.flag = 1;
   Seg sg{warp * SUB, min(cnt, SUB)};
-  int listed;
-  block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[2], &listed);
+  int listed;  // wtot[3]: its next writer (the list emit) is behind barriers
+  block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[3], &listed);
   const bool ok = sm.flag == 0 && (all || listed >= K);
   if (!ok) {  // block-uniform: record every non-empty pair (two list passes
               // cannot hold more than CAP, so take the exact digit path)

@@ -42,25 +42,10 @@ struct Seg {
   __device__ __forceinline__ int rounds() const { return (cnt + 31) >> 5; }
 };
 
-template <int BLOCK>
-__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, SelectSmem<BLOCK> &sm) {
-  mn = __reduce_min_sync(kFull, mn);
-  mx = __reduce_max_sync(kFull, mx);
-  if (lane_id() == 0) {
-    sm.red[warp_id()] = mn;
-    sm.wtot[1][warp_id()] = static_cast<int>(mx);
-  }
-  __syncthreads();
-  uint32_t a = 0xffffffffu, b = 0u;
-#pragma unroll
-  for (int w = 0; w < BLOCK / 32; ++w) {
-    a = min(a, sm.red[w]);
-    b = max(b, static_cast<uint32_t>(sm.wtot[1][w]));
-  }
-  __syncthreads();
-  mn = a;
-  mx = b;
-}
+// Digit width of the list select.  Lists are short, so the cost of a pass
+// is mostly the scan over the bins: 256 bins per pass keep it small, and
+// the range-relative digits still need few passes.
+constexpr int kListDigit = 8;
 
 // Radix select of the K largest keys among the list entries gk(i) != 0 of
 // this thread's segment.  Outcome as Sel (see satk_device.cuh); the
@@ -82,27 +67,45 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
       ++n;
     }
   }
-  // count through a scan, min/max through reductions
-  int total;
-  block_excl_scan<BLOCK>(n, sm.wtot[2], &total);
-  block_minmax<BLOCK>(mn, mx, sm);
+  // count, min and max in one reduction (one barrier): warp values go to
+  // red / wtot[1] / wtot[2]; the next writer of those arrays (another
+  // list_select, block_min) is behind later barriers
+  mn = __reduce_min_sync(kFull, mn);
+  mx = __reduce_max_sync(kFull, mx);
+  n = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(n)));
+  if (lane == 0) {
+    sm.red[warp_id()] = mn;
+    sm.wtot[1][warp_id()] = static_cast<int>(mx);
+    sm.wtot[2][warp_id()] = n;
+  }
+  __syncthreads();
+  int total = 0;
+  mn = 0xffffffffu;
+  mx = 0u;
+#pragma unroll
+  for (int w = 0; w < BLOCK / 32; ++w) {
+    mn = min(mn, sm.red[w]);
+    mx = max(mx, static_cast<uint32_t>(sm.wtot[1][w]));
+    total += sm.wtot[2][w];
+  }
   Sel r;
   r.tie = false;
   r.take_all = false;
   r.total = total;
+  const uint32_t span = mx - mn;
+  const int b = span == 0u ? 0 : 32 - __clz(span);
+  if (total < K || b == 0) __syncthreads();  // no pass barrier follows
   if (total < K) {
     r.take_all = true;
     r.T = 1u;
     r.need = 0;
     return r;
   }
-  const uint32_t span = mx - mn;
-  const int b = span == 0u ? 0 : 32 - __clz(span);
   int need = K;
   uint32_t prefix = 0u;
   int pbits = 0;
   while (pbits < b) {
-    const int width = (b - pbits) < 11 ? (b - pbits) : 11;
+    const int width = (b - pbits) < kListDigit ? (b - pbits) : kListDigit;
     const int shift = b - pbits - width;
     const uint32_t dmask = (1u << width) - 1u;
     for (int j = 0; j < sg.rounds(); ++j) {
@@ -115,7 +118,7 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
       }
     }
     __syncthreads();
-    const PassOut p = find_threshold<BLOCK, 2048>(sm, need);
+    const PassOut p = find_threshold<BLOCK, (1 << kListDigit)>(sm, need);
     need -= p.above;
     prefix = (prefix << width) | static_cast<uint32_t>(p.d);
     pbits += width;

@@ -10,8 +10,8 @@
 // (lowest columns first) up to K.
 //
 // One CTA per row, three steps:
-//  1. threshold: a strided sample of the row (4 columns per thread) is
-//     ranked and a key T0 picked so that, with a margin of about four
+//  1. threshold: a sample of the row (4 columns per thread) is ranked (to
+//     24 bits of its key range) and a key T0 picked so that, with a margin of about four
 //     standard deviations of the sampling error, at least K columns of the
 //     row score at or above it.  Rows no longer than the list capacity skip
 //     this and take every valid column.
@@ -100,7 +100,7 @@ __device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
   r = r < 1 ? 1 : (r > S ? S : r);
   __syncwarp();
   const Seg sg{warp * SUB, 32 * SPT};
-  const Sel s = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, r, sm.sel, 2);
+  const Sel s = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, r, sm.sel, 3);
   return s.take_all ? 1u : s.T;
 }
 
@@ -504,8 +504,9 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear
   Seg sg = collect_filtered<T, BLOCK, SUB, ALIGN, 4>(xr, end, t0f, sm);
+  // wtot[3]: its next writer (the list emit) is behind the select's barriers
   int total;
-  block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[2], &total);
+  block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[3], &total);
   const bool ok = sm.flag == 0 && (all || total >= K);
   if (!ok) {  // block-uniform
     __syncthreads();
