@@ -88,6 +88,12 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   return r;
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 by the copy engine: no registers,
+// no completion to wait for.  p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------ block scan --
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

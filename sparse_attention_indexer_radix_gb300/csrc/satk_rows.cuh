@@ -201,10 +201,40 @@ struct ThresholdOf<uint16_t> {
   __device__ __forceinline__ __nv_bfloat162 arg() const { return t2; }
 };
 
+// The warp's stretch of 8-element groups: [g0, g1) of end / 8 groups.
+template <int BLOCK>
+__device__ __forceinline__ void warp_stretch(int end, int &g0, int &g1) {
+  constexpr int NW = BLOCK / 32;
+  const int ngroups = end / 8;
+  const int per = (ngroups + NW - 1) / NW;
+  g0 = min(ngroups, warp_id() * per);
+  g1 = min(ngroups, g0 + per);
+}
+
+// L2 prefetch of groups [ga, gb) of the warp's stretch (16-byte rows only),
+// issued by lane 0, split in pieces of at most 64 KB.
+template <typename T, int ALIGN>
+__device__ __forceinline__ void prefetch_groups(const T *__restrict__ xr, int ga, int gb) {
+  if constexpr (ALIGN != 0) {
+    if (lane_id() == 0 && ga < gb) {
+      constexpr uint32_t GB = 8 * sizeof(T);  // bytes per group (16 or 32)
+      const char *p = reinterpret_cast<const char *>(xr) + static_cast<size_t>(ga) * GB;
+      uint32_t left = static_cast<uint32_t>(gb - ga) * GB;
+      while (left != 0u) {
+        const uint32_t piece = left < 65536u ? left : 65536u;
+        prefetch_l2(p, piece);
+        p += piece;
+        left -= piece;
+      }
+    }
+  }
+}
+
 // Every warp streams its own contiguous stretch of 8-element groups (one
 // group per lane, U per lane in flight) and records the columns whose score
 // compares >= the threshold, with their keys, in its list segment, in
-// column order.  Per-lane counts of each batch go
+// column order.  The copy engine keeps the L2 PF batches ahead of the
+// warp's loads (the first ones were requested before the threshold step).  Per-lane counts of each batch go
 // through one packed warp prefix scan.  The < 8 ragged columns at the end
 // go to the last warp.  Returns the segment; sets sm.flag on overflow.
 template <typename T, int BLOCK, int SUB, int ALIGN, int U>
@@ -212,15 +242,17 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
                                                 ListSmem<BLOCK, SUB> &sm) {
   static_assert(U % 2 == 0, "counts are packed two per word");
   constexpr int NW = BLOCK / 32;
+  constexpr int PF = 2;  // batches prefetched ahead
   const int lane = lane_id(), warp = warp_id();
   const int ngroups = end / 8;
-  const int per = (ngroups + NW - 1) / NW;
-  const int g0 = min(ngroups, warp * per), g1 = min(ngroups, g0 + per);
+  int g0, g1;
+  warp_stretch<BLOCK>(end, g0, g1);
   uint32_t *lk = sm.key + warp * SUB;
   uint32_t *lv = sm.val + warp * SUB;
   const ThresholdOf<T> thr(t0f);
   int cnt = 0;
   for (int gb = g0; gb < g1; gb += 32 * U) {
+    prefetch_groups<T, ALIGN>(xr, min(g1, gb + PF * 32 * U), min(g1, gb + (PF + 1) * 32 * U));
     Group8<T, ALIGN> grp[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -494,7 +526,13 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   constexpr int KB = KeyOf<T>::kBits;
   constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
   constexpr bool VECLOAD = ALIGN != 0;
+  constexpr int U = 4;  // groups per lane per batch of the filtered pass
   const bool all = end <= CAP;
+  {  // start the copy engine on the first batches of this warp's stretch
+    int g0, g1;
+    warp_stretch<BLOCK>(end, g0, g1);
+    prefetch_groups<T, ALIGN>(xr, g0, min(g1, g0 + 2 * 32 * U));
+  }
   float t0f;
   if (all) {
     t0f = __uint_as_float(0xff800000u);  // -inf: every valid column
@@ -503,7 +541,7 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   }
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear
-  Seg sg = collect_filtered<T, BLOCK, SUB, ALIGN, 4>(xr, end, t0f, sm);
+  Seg sg = collect_filtered<T, BLOCK, SUB, ALIGN, U>(xr, end, t0f, sm);
   // wtot[3]: its next writer (the list emit) is behind the select's barriers
   int total;
   block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[3], &total);
