@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   uint32_t *lk = sm.key + warp * SUB;
   uint32_t *lv = sm.val + warp * SUB;
   int cnt = 0;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;  // range of the keys written
   for (int gr = g0; gr < g1;) {  // runs inside one rank (warp-uniform)
     const int r = gr / gpr;
     const int rend = min(g1, (r + 1) * gpr);
@@ -293,8 +294,11 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
           for (int s = 0; s < 4; ++s) {
             const int pos = pos0 + __popc(mm & ((1u << s) - 1u));
             if (((mm >> s) & 1u) && pos < SUB) {
-              lk[pos] = key_f32(grp[u].w[2 * s]);
+              const uint32_t k = key_f32(grp[u].w[2 * s]);
+              lk[pos] = k;
               lv[pos] = grp[u].w[2 * s + 1];
+              kmn = min(kmn, k);
+              kmx = max(kmx, k);
             }
           }
         }
@@ -305,6 +309,7 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   }
   if (cnt > SUB && lane == 0) sm.flag = 1;
   Seg sg{warp * SUB, min(cnt, SUB)};
+  const WarpStats st{min(cnt, SUB), __reduce_min_sync(kFull, kmn), __reduce_max_sync(kFull, kmx)};
   int listed;  // wtot[3]: its next writer (the list emit) is behind barriers
   block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[3], &listed);
   const bool ok = sm.flag == 0 && (all || listed >= K);
@@ -372,7 +377,8 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   __syncwarp();
 
   // ---- select: by score, then by global id among ties with the K-th
-  const Sel s1 = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, K, sm.sel);
+  const Sel s1 = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, K, sm.sel, 8,
+                                    ok ? st : stats_unknown());
   uint32_t t2 = 0u;
   bool use2 = false, tie2 = false;
   if (!s1.take_all && s1.tie) {

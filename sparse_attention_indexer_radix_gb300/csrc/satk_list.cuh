@@ -42,37 +42,57 @@ struct Seg {
   __device__ __forceinline__ int rounds() const { return (cnt + 31) >> 5; }
 };
 
-// Digit width of the list select.  Lists are short, so the cost of a pass
-// is mostly the scan over the bins: 256 bins per pass keep it small, and
-// the range-relative digits still need few passes.
-constexpr int kListDigit = 8;
+// Count, smallest and largest key of one warp's list entries, when the
+// pass that wrote them already knows them (warp-uniform values); n < 0
+// means unknown.
+struct WarpStats {
+  int n;
+  uint32_t mn, mx;
+  __device__ __forceinline__ bool known() const { return n >= 0; }
+};
+__device__ __forceinline__ WarpStats stats_unknown() { return WarpStats{-1, 0u, 0u}; }
+
+// Digit width of the list select: a pass costs one walk over the list plus
+// one scan over the bins.  Short lists take 8-bit digits (cheap scans),
+// longer ones 11-bit digits (fewer walks).
+constexpr int kListDigitShort = 8;
+constexpr int kListDigitLong = 11;
+constexpr int kListLong = 1024;
 
 // Radix select of the K largest keys among the list entries gk(i) != 0 of
 // this thread's segment.  Outcome as Sel (see satk_device.cuh); the
 // threshold T is an absolute key.  gk may return 0 to drop an entry.
 // With max_passes, the digit passes stop early and T is the start of the
-// threshold digit (at least K keys are >= T).
+// threshold digit (at least K keys are >= T).  With pre known, the warp's
+// count and key range come from the caller instead of a walk over the list
+// (gk must then be non-zero exactly on those entries).
 template <int BLOCK, class GetKey>
 __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &sm,
-                           int max_passes = 8) {
+                           int max_passes = 8, WarpStats pre = stats_unknown()) {
   const int lane = lane_id();
   uint32_t mn = 0xffffffffu, mx = 0u;
   int n = 0;
-  for (int j = 0; j < sg.rounds(); ++j) {
-    const int i = j * 32 + lane;
-    const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
-    if (k != 0u) {
-      mn = min(mn, k);
-      mx = max(mx, k);
-      ++n;
+  if (pre.known()) {
+    n = pre.n;
+    mn = pre.mn;
+    mx = pre.mx;
+  } else {
+    for (int j = 0; j < sg.rounds(); ++j) {
+      const int i = j * 32 + lane;
+      const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
+      if (k != 0u) {
+        mn = min(mn, k);
+        mx = max(mx, k);
+        ++n;
+      }
     }
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    n = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(n)));
   }
   // count, min and max in one reduction (one barrier): warp values go to
   // red / wtot[1] / wtot[2]; the next writer of those arrays (another
   // list_select, block_min) is behind later barriers
-  mn = __reduce_min_sync(kFull, mn);
-  mx = __reduce_max_sync(kFull, mx);
-  n = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(n)));
   if (lane == 0) {
     sm.red[warp_id()] = mn;
     sm.wtot[1][warp_id()] = static_cast<int>(mx);
@@ -104,8 +124,9 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
   int need = K;
   uint32_t prefix = 0u;
   int pbits = 0;
+  const int digit = total > kListLong ? kListDigitLong : kListDigitShort;
   while (pbits < b) {
-    const int width = (b - pbits) < kListDigit ? (b - pbits) : kListDigit;
+    const int width = (b - pbits) < digit ? (b - pbits) : digit;
     const int shift = b - pbits - width;
     const uint32_t dmask = (1u << width) - 1u;
     for (int j = 0; j < sg.rounds(); ++j) {
@@ -118,7 +139,9 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
       }
     }
     __syncthreads();
-    const PassOut p = find_threshold<BLOCK, (1 << kListDigit)>(sm, need);
+    const PassOut p = digit == kListDigitLong
+                          ? find_threshold<BLOCK, (1 << kListDigitLong)>(sm, need)
+                          : find_threshold<BLOCK, (1 << kListDigitShort)>(sm, need);
     need -= p.above;
     prefix = (prefix << width) | static_cast<uint32_t>(p.d);
     pbits += width;
@@ -138,33 +161,53 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
 
 // Ordered compaction over the list segments: cls(i) = 0 skip, 1 group A,
 // 2 group B for absolute entry i; emitA/emitB(rank, i, tot) as in
-// ordered_emit.  Two barriers.
+// ordered_emit.  The counting walk keeps each round's two ballots (in the
+// zero histogram, 64 words per warp, cleared again afterwards) so the
+// writing walk need not classify again.  Two barriers.
 template <int BLOCK, class Cls, class EmitA, class EmitB>
 __device__ int2 list_emit(Cls cls, const Seg &sg, EmitA emitA, EmitB emitB, SelectSmem<BLOCK> &sm) {
+  static_assert(BLOCK / 32 * 64 <= 2048, "ballot store exceeds the histogram");
   const int lane = lane_id();
   const unsigned lt = (1u << lane) - 1u;
+  uint32_t *bal = sm.hist + warp_id() * 64;
+  const int R = sg.rounds();
   int ca = 0, cb = 0;
-  for (int j = 0; j < sg.rounds(); ++j) {
+  for (int j = 0; j < R; ++j) {
     const int i = j * 32 + lane;
     const int c = i < sg.cnt ? cls(sg.base + i) : 0;
-    ca += __popc(__ballot_sync(kFull, c == 1));
-    cb += __popc(__ballot_sync(kFull, c == 2));
+    const unsigned ba = __ballot_sync(kFull, c == 1);
+    const unsigned bb = __ballot_sync(kFull, c == 2);
+    if (lane == 0 && j < 32) {
+      bal[2 * j] = ba;
+      bal[2 * j + 1] = bb;
+    }
+    ca += __popc(ba);
+    cb += __popc(bb);
   }
   int total;
   const unsigned base =
       (unsigned)block_warp_prefix<BLOCK>((ca << 16) | cb, sm.wtot[3], &total);
   const int2 tot = make_int2((int)((unsigned)total >> 16), (int)((unsigned)total & 0xffffu));
   int ra = (int)(base >> 16), rb = (int)(base & 0xffffu);
-  for (int j = 0; j < sg.rounds(); ++j) {
+  for (int j = 0; j < R; ++j) {
     const int i = j * 32 + lane;
-    const int c = i < sg.cnt ? cls(sg.base + i) : 0;
-    const unsigned ba = __ballot_sync(kFull, c == 1);
-    const unsigned bb = __ballot_sync(kFull, c == 2);
-    if (c == 1) emitA(ra + __popc(ba & lt), sg.base + i, tot);
-    if (c == 2) emitB(rb + __popc(bb & lt), sg.base + i, tot);
+    unsigned ba, bb;
+    if (j < 32) {
+      ba = bal[2 * j];
+      bb = bal[2 * j + 1];
+    } else {
+      const int c = i < sg.cnt ? cls(sg.base + i) : 0;
+      ba = __ballot_sync(kFull, c == 1);
+      bb = __ballot_sync(kFull, c == 2);
+    }
+    if ((ba >> lane) & 1u) emitA(ra + __popc(ba & lt), sg.base + i, tot);
+    if ((bb >> lane) & 1u) emitB(rb + __popc(bb & lt), sg.base + i, tot);
     ra += __popc(ba);
     rb += __popc(bb);
   }
+  __syncwarp();
+  bal[lane] = 0u;
+  bal[lane + 32] = 0u;
   __syncthreads();
   return tot;
 }
@@ -173,9 +216,9 @@ __device__ int2 list_emit(Cls cls, const Seg &sg, EmitA emitA, EmitB emitB, Sele
 // then entries equal to it in list order up to K, then fill(pos) up to K.
 template <int BLOCK, int SUB, class Put, class Fill>
 __device__ void list_topk_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, Put put,
-                               Fill fill) {
+                               Fill fill, WarpStats pre = stats_unknown()) {
   auto gk = [&](int i) { return sm.key[i]; };
-  const Sel sel = list_select<BLOCK>(gk, sg, K, sm.sel);
+  const Sel sel = list_select<BLOCK>(gk, sg, K, sm.sel, 8, pre);
   uint32_t v;
   if (sel.take_all) {
     v = 0u;

@@ -239,7 +239,7 @@ __device__ __forceinline__ void prefetch_groups(const T *__restrict__ xr, int ga
 // go to the last warp.  Returns the segment; sets sm.flag on overflow.
 template <typename T, int BLOCK, int SUB, int ALIGN, int U>
 __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int end, float t0f,
-                                                ListSmem<BLOCK, SUB> &sm) {
+                                                ListSmem<BLOCK, SUB> &sm, WarpStats &st) {
   static_assert(U % 2 == 0, "counts are packed two per word");
   constexpr int NW = BLOCK / 32;
   constexpr int PF = 2;  // batches prefetched ahead
@@ -251,6 +251,7 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
   uint32_t *lv = sm.val + warp * SUB;
   const ThresholdOf<T> thr(t0f);
   int cnt = 0;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;  // range of the keys written
   for (int gb = g0; gb < g1; gb += 32 * U) {
     prefetch_groups<T, ALIGN>(xr, min(g1, gb + PF * 32 * U), min(g1, gb + (PF + 1) * 32 * U));
     Group8<T, ALIGN> grp[U];
@@ -288,8 +289,11 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
         const int s = __ffs(mm) - 1;
         mm &= mm - 1u;
         if (pos < SUB) {
-          lk[pos] = key_of_raw<T>(grp[u].raw(s));
+          const uint32_t k = key_of_raw<T>(grp[u].raw(s));
+          lk[pos] = k;
           lv[pos] = static_cast<uint32_t>(c0 + s);
+          kmn = min(kmn, k);
+          kmx = max(kmx, k);
         }
         ++pos;
       }
@@ -303,12 +307,18 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
     const unsigned b = __ballot_sync(kFull, keep);
     const int pos = cnt + __popc(b & ((1u << lane) - 1u));
     if (keep && pos < SUB) {
-      lk[pos] = key_of_raw<T>(rw);
+      const uint32_t k = key_of_raw<T>(rw);
+      lk[pos] = k;
       lv[pos] = static_cast<uint32_t>(c);
+      kmn = min(kmn, k);
+      kmx = max(kmx, k);
     }
     cnt += __popc(b);
   }
   if (cnt > SUB && lane == 0) sm.flag = 1;
+  st.n = min(cnt, SUB);
+  st.mn = __reduce_min_sync(kFull, kmn);
+  st.mx = __reduce_max_sync(kFull, kmx);
   return Seg{warp * SUB, min(cnt, SUB)};
 }
 
@@ -541,7 +551,8 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   }
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear
-  Seg sg = collect_filtered<T, BLOCK, SUB, ALIGN, U>(xr, end, t0f, sm);
+  WarpStats st;
+  Seg sg = collect_filtered<T, BLOCK, SUB, ALIGN, U>(xr, end, t0f, sm, st);
   // wtot[3]: its next writer (the list emit) is behind the select's barriers
   int total;
   block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[3], &total);
@@ -550,7 +561,7 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
     __syncthreads();
     sg = collect_exact<T, BLOCK, SUB, VECLOAD>(xr, end, K, sm);
   }
-  list_topk_emit<BLOCK, SUB>(sm, sg, K, put, fill);
+  list_topk_emit<BLOCK, SUB>(sm, sg, K, put, fill, ok ? st : stats_unknown());
 }
 
 }  // namespace satk
