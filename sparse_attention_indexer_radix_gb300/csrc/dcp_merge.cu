@@ -282,6 +282,12 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
       for (int u = 0; u < U; ++u) pk |= static_cast<uint32_t>(__popc(m[u])) << (8 * u);
       const uint32_t incl = static_cast<uint32_t>(warp_incl_scan(static_cast<int>(pk)));
       const uint32_t tot = __shfl_sync(kFull, incl, 31);
+      const int btot = static_cast<int>((tot & 0xffu) + ((tot >> 8) & 0xffu) +
+                                        ((tot >> 16) & 0xffu) + (tot >> 24));
+      if (cnt + btot > SUB) {  // warp-uniform: the segment overflows
+        cnt += btot;
+        break;
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t lc = static_cast<uint32_t>(__popc(m[u]));
@@ -293,8 +299,8 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
             const int pos = pos0 + __popc(mm & ((1u << s) - 1u));
-            if (((mm >> s) & 1u) && pos < SUB) {
-              const uint32_t k = key_f32(grp[u].w[2 * s]);
+            if ((mm >> s) & 1u) {
+              const uint32_t k = key_f32_num(grp[u].w[2 * s]);
               lk[pos] = k;
               lv[pos] = grp[u].w[2 * s + 1];
               kmn = min(kmn, k);
@@ -305,7 +311,7 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
         cnt += static_cast<int>((tot >> (8 * u)) & 0xffu);
       }
     }
-    gr = rend;
+    gr = cnt > SUB ? g1 : rend;  // stop at an overflow
   }
   if (cnt > SUB && lane == 0) sm.flag = 1;
   Seg sg{warp * SUB, min(cnt, SUB)};

@@ -36,6 +36,15 @@ __device__ __forceinline__ uint32_t key_f32(uint32_t b) {
 }
 
 // bf16 pattern in the low 16 bits -> ord16 << 16 (0 for NaN).
+// The same keys for values known not to be NaN (they passed a >= compare):
+// flip every bit of a negative value, only the sign bit of the others.
+__device__ __forceinline__ uint32_t key_f32_num(uint32_t b) {
+  return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t key_bf16_num(uint32_t h) {
+  return key_f32_num(h << 16) & 0xffff0000u;
+}
+
 __device__ __forceinline__ uint32_t key_bf16(uint32_t h) {
   h &= 0xffffu;
   if ((h & 0x7fffu) > 0x7f80u) return 0u;  // NaN

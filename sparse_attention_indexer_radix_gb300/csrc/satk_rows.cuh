@@ -52,6 +52,13 @@ __device__ __forceinline__ uint32_t key_of_raw(uint32_t raw) {
     return key_bf16(raw);
 }
 template <typename T>
+__device__ __forceinline__ uint32_t key_of_num(uint32_t raw) {  // raw not NaN
+  if constexpr (std::is_same<T, float>::value)
+    return key_f32_num(raw);
+  else
+    return key_bf16_num(raw);
+}
+template <typename T>
 __device__ __forceinline__ uint32_t load_raw(const T *p) {
   if constexpr (std::is_same<T, float>::value)
     return __float_as_uint(__ldg(p));
@@ -274,10 +281,16 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
     }
     if (!__any_sync(kFull, any != 0u)) continue;
     uint32_t incl[U / 2], tot[U / 2];
+    int btot = 0;
 #pragma unroll
     for (int j = 0; j < U / 2; ++j) {
       incl[j] = static_cast<uint32_t>(warp_incl_scan(static_cast<int>(pk[j])));
       tot[j] = __shfl_sync(kFull, incl[j], 31);
+      btot += static_cast<int>((tot[j] & 0xffffu) + (tot[j] >> 16));
+    }
+    if (cnt + btot > SUB) {  // warp-uniform: the segment overflows
+      cnt += btot;
+      break;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -288,26 +301,24 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
       while (mm != 0u) {
         const int s = __ffs(mm) - 1;
         mm &= mm - 1u;
-        if (pos < SUB) {
-          const uint32_t k = key_of_raw<T>(grp[u].raw(s));
-          lk[pos] = k;
-          lv[pos] = static_cast<uint32_t>(c0 + s);
-          kmn = min(kmn, k);
-          kmx = max(kmx, k);
-        }
+        const uint32_t k = key_of_num<T>(grp[u].raw(s));
+        lk[pos] = k;
+        lv[pos] = static_cast<uint32_t>(c0 + s);
+        kmn = min(kmn, k);
+        kmx = max(kmx, k);
         ++pos;
       }
       cnt += static_cast<int>((tot[u >> 1] >> (16 * (u & 1))) & 0xffffu);
     }
   }
-  if (warp == NW - 1 && ngroups * 8 < end) {  // ragged columns
+  if (warp == NW - 1 && ngroups * 8 < end && cnt <= SUB) {  // ragged columns
     const int c = ngroups * 8 + lane;
     const uint32_t rw = c < end ? load_raw(xr + c) : 0u;
     const bool keep = c < end && as_float<T>(rw) >= t0f;
     const unsigned b = __ballot_sync(kFull, keep);
     const int pos = cnt + __popc(b & ((1u << lane) - 1u));
     if (keep && pos < SUB) {
-      const uint32_t k = key_of_raw<T>(rw);
+      const uint32_t k = key_of_num<T>(rw);
       lk[pos] = k;
       lv[pos] = static_cast<uint32_t>(c);
       kmn = min(kmn, k);
