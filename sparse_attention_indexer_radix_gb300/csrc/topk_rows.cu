@@ -8,8 +8,11 @@
 // a shared-memory list, exact select on the list).
 #include <climits>
 
+#include <cmath>
+
 #include "satk_host.hpp"
 #include "satk_rows.cuh"
+#include "satk_warp.cuh"
 
 namespace satk {
 namespace {
@@ -59,10 +62,56 @@ int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_en
   return launch_status();
 }
 
+// Short rows: one warp per row (satk_warp.cuh), kWarpRowsPerCta rows per
+// CTA, seven CTAs per SM (their workspaces fill the shared memory).
+template <typename T, int ALIGN>
+__global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
+    topk_rows_warp_kernel(const T *__restrict__ x, int64_t rows, int64_t ld, int cols,
+                          const int32_t *__restrict__ row_ends, int K,
+                          int32_t *__restrict__ out, int64_t ld_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int warp = warp_id();
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpRowsPerCta + warp;
+  if (row >= rows) return;  // warp-uniform; the warps never synchronise
+  WarpRowSmem &ws = reinterpret_cast<WarpRowSmem *>(smem_raw)[warp];
+  for (int i = lane_id(); i < 256; i += 32) ws.hist[i] = 0u;
+  __syncwarp();
+  warp_topk_row<T, ALIGN>(x + row * ld, row_end_of(row_ends, row, cols), K, out + row * ld_out,
+                          ws);
+}
+
+template <typename T, int ALIGN>
+int launch_warp(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
+                int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_warp_kernel<T, ALIGN>;
+  const size_t smem = sizeof(WarpRowSmem) * kWarpRowsPerCta;
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  const int64_t grid = (rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta;
+  kern<<<dim3(static_cast<unsigned>(grid)), 32 * kWarpRowsPerCta, smem, st>>>(
+      x, rows, ld, cols, row_ends, K, out, ld_out);
+  return launch_status();
+}
+
+// Whether a row of `cols` columns keeps its sampled candidate list within
+// one warp's kWarpList entries: the expected list K r / mu (r and mu as in
+// the sample step) plus four standard deviations (about list / sqrt(r)) of
+// the r-th sample order statistic.  Rows that still overflow take the exact
+// path, so this only decides speed.
+inline bool warp_rows_fit(int cols, int K) {
+  if (K > 512 || cols > 65536) return false;
+  if (cols <= kWarpList) return true;
+  const double mu = static_cast<double>(K) * kWarpSample / cols;
+  const double r = std::ceil(mu + 4.0 * std::sqrt(mu) + 4.0);
+  const double list = K * r / mu;
+  return list + 4.0 * list / std::sqrt(r) <= kWarpList;
+}
+
 // The list holds (BLOCK/32) warps x SUB candidates.
 template <typename T, int ALIGN>
 int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
+  if (warp_rows_fit(cols, K))
+    return launch_warp<T, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
   if (cols <= kShortCols && K <= 512)
     return launch<T, kShortBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
   if (K <= 1024)

@@ -120,6 +120,29 @@ def test_topk_special_values_and_ties():
         assert_rows_equal(got, want, f"specials bf16 k={k}")
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("ld", [8192, 8195])
+def test_topk_warp_rows_edges(dtype, ld):
+    """Rows short enough for one warp per row: row ends around the list
+    size and the sample's run layout, a clustered top block the sample can
+    miss, and few-level rows whose list overflows (the exact path)."""
+    rows, cols = 40, 8192
+    x, _ = inputs.prefill(rows=rows, cols=cols, seed=ld, dtype=torch.float32)
+    g = torch.Generator().manual_seed(ld)
+    x[30, 3000:3600] = 10.0 + torch.rand(600, generator=g)   # clustered top block
+    x[31, 5000:5300] = 7.0                                   # clustered, tied
+    x[32] = torch.randint(0, 3, (cols,), generator=g).float()  # three levels
+    x[33] = torch.randint(0, 40, (cols,), generator=g).float()
+    x[34, ::3] = float("nan")
+    ends = torch.full((rows,), cols, dtype=torch.int32)
+    ends[:12] = torch.tensor([0, 31, 32, 511, 1024, 1025, 1046, 1100, 1535, 1536, 1537, 4097],
+                             dtype=torch.int32)
+    x = x.to(dtype)
+    for k in (1, 100, 512):
+        got, want = run_topk(x, k, ends, k + 5, ld_x=ld)
+        assert_rows_equal(got, want, f"warp rows {dtype} ld={ld} k={k}")
+
+
 @pytest.mark.parametrize("mode", ["plus100", "times1e-8"])
 def test_topk_concentrated_distributions(mode):
     x, ends = inputs.prefill_shifted(64, 8192, mode)
