@@ -232,7 +232,7 @@ def timed_calls(fn, reps, flush):
     return statistics.median(times)
 
 
-STAGES = ("pairs", "decode", "adversarial")
+STAGES = ("pairs", "decode", "adversarial", "robust")
 
 
 def stage_figures(dev, flush, peak, which=STAGES):
@@ -244,6 +244,8 @@ def stage_figures(dev, flush, peak, which=STAGES):
         st.update(_stage_decode(dev, flush, peak, satk))
     if "adversarial" in which:
         st.update(_stage_adversarial(dev, flush, peak, satk))
+    if "robust" in which:
+        st.update(_stage_robust(dev, flush, peak, satk))
     return st
 
 
@@ -311,6 +313,38 @@ def _stage_adversarial(dev, flush, peak, satk):
     st["adversarial_bf16_256x131072_K2048"] = {
         "us": ms * 1e3, "rows_per_s": 256 / (ms * 1e-3), "gbs": nb / (ms * 1e-3) / 1e9,
         "frac": nb / (ms * 1e-3) / 1e9 / peak}
+    return st
+
+
+# The prefill page's other shapes (the query rows x logits columns of its
+# captured chunks, here on synthetic N(0,1) logits) and its distribution
+# ablation at 8192 x 8192: fp32, causal row ends, K = 512.
+ROBUST_SHAPES = ((8192, 4096), (8192, 8192), (2048, 25600), (2048, 51200), (1310, 102400))
+ROBUST_MODES = ("plus100", "times1e-8")
+
+
+def _stage_robust(dev, flush, peak, satk):
+    st = {}
+
+    def one(name, x, ends):
+        rows = x.shape[0]
+        out = torch.empty((rows, K), dtype=torch.int32, device=dev)
+        fn = lambda: satk.topk_rows(x, K, row_ends=ends, out=out)  # noqa: E731
+        for _ in range(3):
+            fn()
+        ms = timed_calls(fn, 10, flush)
+        nb = int(ends.clamp(min=0).sum().item()) * 4 + rows * K * 4
+        st[name] = {"us": ms * 1e3, "rows_per_s": rows / (ms * 1e-3),
+                    "gbs": nb / (ms * 1e-3) / 1e9, "frac": nb / (ms * 1e-3) / 1e9 / peak}
+
+    for i, (rows, cols) in enumerate(ROBUST_SHAPES):
+        x, ends = inputs.prefill(rows=rows, cols=cols, seed=1250 + i, device=dev)
+        one(f"shape_{rows}x{cols}_f32_K512", x, ends)
+        del x
+    for mode in ROBUST_MODES:
+        x, ends = inputs.prefill_shifted(8192, 8192, mode, device=dev)
+        one(f"dist_{mode}_8192x8192_f32_K512", x, ends)
+        del x
     return st
 
 

@@ -249,7 +249,7 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
                                                 ListSmem<BLOCK, SUB> &sm, WarpStats &st) {
   static_assert(U % 2 == 0, "counts are packed two per word");
   constexpr int NW = BLOCK / 32;
-  constexpr int PF = 2;  // batches prefetched ahead
+  constexpr int PF = 1;  // batches prefetched ahead (more is evicted before use)
   const int lane = lane_id(), warp = warp_id();
   const int ngroups = end / 8;
   int g0, g1;

@@ -8,7 +8,7 @@
 //  1. threshold from a sample of kWarpSample columns (6 runs of 256);
 //  2. one filtered pass that records keys and columns of the columns at or
 //     above it in the warp's list, in column order, with the copy engine
-//     two batches ahead of the loads (bulk L2 prefetch);
+//     one batch ahead of the loads (bulk L2 prefetch);
 //  3. exact select on the list (8-bit digits relative to the list's key
 //     range, a 256-bin histogram per warp) and the ordered emit: ids with
 //     key > v in ascending column order, then ids with key == v, -1 after.
@@ -214,7 +214,7 @@ __device__ __forceinline__ bool warp_collect(const T *__restrict__ xr, int end, 
   uint32_t kmn = 0xffffffffu, kmx = 0u;
   bool over = false;
   for (int gb = 0; gb < ngroups; gb += 32 * U) {
-    prefetch_groups<T, ALIGN>(xr, min(ngroups, gb + 2 * 32 * U), min(ngroups, gb + 3 * 32 * U));
+    prefetch_groups<T, ALIGN>(xr, min(ngroups, gb + 32 * U), min(ngroups, gb + 2 * 32 * U));
     Group8<T, ALIGN> grp[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -411,8 +411,8 @@ template <typename T, int ALIGN>
 __device__ void warp_topk_row(const T *__restrict__ xr, int end, int K, int32_t *__restrict__ o,
                               WarpRowSmem &ws) {
   constexpr int KB = KeyOf<T>::kBits;
-  // the copy engine starts on the first two batches of the filtered pass
-  prefetch_groups<T, ALIGN>(xr, 0, min(end / 8, 2 * 32 * 4));
+  // the copy engine starts on the first batch of the filtered pass
+  prefetch_groups<T, ALIGN>(xr, 0, min(end / 8, 32 * 4));
   const bool all = end <= kWarpList;
   float t0f = __uint_as_float(0xff800000u);  // -inf: every valid column
   if (!all) t0f = threshold_float<KB>(warp_sample_threshold<T, ALIGN>(xr, end, K, ws));

@@ -169,21 +169,45 @@ def test_adversarial_workload_full():
 def test_prefill_full_size_sampled(cols):
     """The prefill workload at full size, in the launch configuration the
     benchmark times; rows sampled for the oracle, properties on all rows."""
-    rows, k, ld_out = inputs.PREFILL_ROWS, inputs.PREFILL_K, inputs.PREFILL_LD_OUT
-    x, ends = inputs.prefill(rows=rows, cols=cols, seed=1236, device=DEV)
+    x, ends = inputs.prefill(rows=inputs.PREFILL_ROWS, cols=cols, seed=1236, device=DEV)
+    check_full_size_sampled(x, ends, inputs.PREFILL_LD_OUT, seed=cols, what=f"prefill {cols}")
+
+
+@pytest.mark.parametrize("rows,cols", [(8192, 4096), (8192, 8192), (2048, 25600), (2048, 51200),
+                                       (1310, 102400)])
+def test_prefill_page_shapes_sampled(rows, cols):
+    """The other query-row x column shapes the benchmark reports, at full size."""
+    x, ends = inputs.prefill(rows=rows, cols=cols, seed=1250, device=DEV)
+    check_full_size_sampled(x, ends, inputs.PREFILL_K, seed=rows + cols, what=f"{rows}x{cols}")
+
+
+@pytest.mark.parametrize("mode", ["plus100", "times1e-8"])
+def test_prefill_shifted_full_size_sampled(mode):
+    """The distribution ablation the benchmark reports, 8192 x 8192, at full size."""
+    x, ends = inputs.prefill_shifted(8192, 8192, mode, device=DEV)
+    check_full_size_sampled(x, ends, inputs.PREFILL_K, seed=7, what=mode)
+
+
+def check_full_size_sampled(x, ends, ld_out, seed, what):
+    rows, k = x.shape[0], inputs.PREFILL_K
     out = torch.full((rows, ld_out), CANARY, dtype=torch.int32, device=DEV)
     satk.topk_rows(x, k, row_ends=ends, out=out)
     got = out.cpu().numpy()
-    sample = np.unique(np.concatenate([[0, 1, rows - 1], np.random.default_rng(cols).integers(0, rows, 40)]))
+    sample = np.unique(np.concatenate([[0, 1, rows - 1], np.random.default_rng(seed).integers(0, rows, 40)]))
     xs = x[sample].cpu().numpy()
     want = np.full((len(sample), ld_out), CANARY, dtype=np.int32)
     oracle.topk_rows(xs, k, row_ends=ends[sample].cpu().numpy(), out=want)
-    assert_rows_equal(got[sample], want, f"prefill {cols} sampled")
-    # every row: ids in range, unique, -1 free, canaries intact
+    assert_rows_equal(got[sample], want, f"{what} sampled")
+    # every row (N(0,1): no NaN): min(end, k) ids in [0, end), unique, then
+    # -1, canaries intact
     assert np.all(got[:, k:] == CANARY)
-    e = ends.cpu().numpy()
-    assert np.all(got[:, :k] >= 0) and np.all(got[:, :k] < e[:, None])
-    srt = np.sort(got[:, :k], axis=1)
+    e = np.clip(ends.cpu().numpy().astype(np.int64), 0, x.shape[1])
+    nsel = np.minimum(e, k)
+    pos = np.arange(k)[None, :]
+    ids = got[:, :k]
+    sel = pos < nsel[:, None]
+    assert np.all(np.where(sel, (ids >= 0) & (ids < e[:, None]), ids == -1))
+    srt = np.sort(np.where(sel, ids, -1 - pos), axis=1)
     assert np.all(srt[:, 1:] != srt[:, :-1])
 
 
