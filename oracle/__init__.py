@@ -64,8 +64,10 @@ def _load():
                                                 vp, vp, ctypes.c_int]
             lib.oracle_rescue.argtypes = [vp, i32, i64, i32, i32, vp, i64, i64,
                                           vp, vp, vp, vp, i64, vp, ctypes.c_int]
+            lib.oracle_emit_rows.argtypes = [vp, i64, i32, i64, i32, i32, vp, vp, i64,
+                                             i64, i32, i32, i64, vp, i64, vp, vp]
             for f in ("oracle_topk_rows", "oracle_dcp_pack", "oracle_merge_pairs",
-                      "oracle_merge_packed", "oracle_rescue"):
+                      "oracle_merge_packed", "oracle_rescue", "oracle_emit_rows"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -186,3 +188,28 @@ def rescue(packed, k, logits_bits, sat_word, ids, row_ends=None, recv=None,
                                _ptr(status), nthreads)
     _check(rc, "rescue")
     return ids, recv, int(status[0])
+
+
+def emit_rows(ids, W, rank, req_id, block_table, block_size, stride_rows,
+              max_blocks=None, ld_rows=None):
+    """This rank's physical KV rows of the selected ids ([T, k] int32): the
+    owned ids (gid % W == rank) whose block gid // W // block_size is below
+    ``max_blocks`` (default: the table's width), mapped through
+    ``block_table`` ([R, width] int32) and ``req_id`` ([T] int32).  Returns
+    (rows_out [T, ld_rows] int32 with columns [k, ld_rows) left at -7,
+    valid_out [T] int32, status)."""
+    i = _c(ids, np.int32)
+    T, k = i.shape
+    rq = _c(req_id, np.int32)
+    bt = _c(block_table, np.int32)
+    R, width = bt.shape
+    max_blocks = width if max_blocks is None else max_blocks
+    ld_rows = k if ld_rows is None else ld_rows
+    rows = np.full((T, ld_rows), -7, dtype=np.int32)
+    valid = np.full(T, -7, dtype=np.int32)
+    status = np.zeros(1, dtype=np.int32)
+    rc = _load().oracle_emit_rows(_ptr(i), T, k, k, W, rank, _ptr(rq), _ptr(bt), R, width,
+                                  max_blocks, block_size, stride_rows, _ptr(rows), ld_rows,
+                                  _ptr(valid), _ptr(status))
+    _check(rc, "emit_rows")
+    return rows, valid, int(status[0])

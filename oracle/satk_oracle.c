@@ -39,7 +39,9 @@
  *    a row with fewer than K valid columns lists them all in ascending
  *    column order; then -1 up to K; columns [K, ld_out) are never written;
  *  - merge output layout: the chosen candidates in ascending flat candidate
- *    order (rank-major, then slot), then -1.
+ *    order (rank-major, then slot), then -1;
+ *  - owned physical rows: in the order of the ids they come from (the owned
+ *    subsequence of a merge output row), then -1 up to k.
  */
 #include <math.h>
 #include <pthread.h>
@@ -594,5 +596,63 @@ int oracle_rescue(const int32_t *packed, int32_t W, int64_t T, int32_t n,
     *status |= s;
   }
   free(row_status);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* owned physical KV rows of the selected tokens                             */
+/* [P2 DCPTopkSelectKernel docstring (emit_rows); dcp_topk_merge_rows        */
+/*  docstring (rows_out, valid_out)]                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Row t: walk ids[t, 0:k) in order.  An id g >= 0 with g % W == rank is a
+ * token of this rank, local index l = g / W, in block b = l / B.  A block
+ * b >= max_blocks (past the block table's width) is dropped; otherwise the
+ * physical row block_table[req_id[t], b] * stride_rows + l % B, taken modulo
+ * 2**32 as a signed 32-bit value (the page computes it in 32-bit integers),
+ * is appended to rows_out[t].  Then -1 up to k (columns [k, ld_rows) are
+ * never written) and valid_out[t] = the count.  A req_id outside
+ * [0, table_rows) appends nothing and sets status bit 4 (reading: the page
+ * does not check it).
+ */
+int oracle_emit_rows(const int32_t *ids, int64_t T, int32_t k, int64_t ld_ids,
+                     int32_t W, int32_t rank, const int32_t *req_id,
+                     const int32_t *block_table, int64_t table_rows,
+                     int64_t ld_table, int32_t max_blocks, int32_t block_size,
+                     int64_t stride_rows, int32_t *rows_out, int64_t ld_rows,
+                     int32_t *valid_out, int32_t *status) {
+  if (!ids || !req_id || !block_table || !rows_out || !valid_out || T < 0 ||
+      k < 1 || ld_ids < k || W < 1 || rank < 0 || rank >= W ||
+      table_rows < 0 || max_blocks < 0 || ld_table < max_blocks ||
+      block_size < 1 || ld_rows < k)
+    return -1;
+  int32_t st = 0;
+  for (int64_t t = 0; t < T; ++t) {
+    const int32_t *id = ids + t * ld_ids;
+    int32_t *out = rows_out + t * ld_rows;
+    const int32_t req = req_id[t];
+    int32_t n = 0;
+    if (req < 0 || (int64_t)req >= table_rows) {
+      st |= 4;
+    } else {
+      const int32_t *table = block_table + (int64_t)req * ld_table;
+      for (int32_t j = 0; j < k; ++j) {
+        const int32_t g = id[j];
+        if (g < 0 || g % W != rank) continue;
+        const int32_t local = g / W;
+        const int32_t b = local / block_size;
+        if (b >= max_blocks) continue;
+        const int64_t phys = (int64_t)table[b] * stride_rows + local % block_size;
+        const uint32_t low = (uint32_t)((uint64_t)phys & 0xFFFFFFFFu);
+        int32_t v;
+        memcpy(&v, &low, sizeof v);
+        out[n++] = v;
+      }
+    }
+    for (int32_t j = n; j < k; ++j) out[j] = -1;
+    valid_out[t] = n;
+  }
+  if (status) *status |= st;
   return 0;
 }

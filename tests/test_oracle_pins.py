@@ -367,3 +367,85 @@ def test_contract_checker_bites():
     packed = oracle.dcp_pack(bits, local)
     with pytest.raises(AssertionError):
         packed_contract(packed, bits, None, 32)
+
+
+# ------------------------------------------------------------- emit_rows --
+
+def _emit_rows_golden():
+    path = os.path.join(os.path.dirname(__file__), "golden", "emit_rows_example.txt")
+    g = {"table": [], "ids": [], "rows": []}
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *vals = line.split()
+        vals = [int(v) for v in vals]
+        if key in g:
+            g[key].append(vals)
+        else:
+            g[key] = vals if len(vals) > 1 else vals[0]
+    return g
+
+
+def test_emit_rows_hand_worked_example():
+    g = _emit_rows_golden()
+    rows, valid, status = oracle.emit_rows(
+        np.array(g["ids"], dtype=np.int32), g["W"], g["rank"],
+        np.array(g["req"], dtype=np.int32), np.array(g["table"], dtype=np.int32),
+        g["block_size"], g["stride_rows"], ld_rows=10)
+    assert rows[:, :8].tolist() == g["rows"]
+    assert np.all(rows[:, 8:] == -7)  # columns past k never written
+    assert valid.tolist() == g["valid"]
+    assert status == g["status"]
+
+
+def test_emit_rows_identity_table_gives_local_ids():
+    """block_table[r][b] = b and stride_rows = B make every physical row the
+    token's own local index gid // W: the owned subsequence, in order."""
+    rng = np.random.default_rng(11)
+    W, B, k, T = 8, 64, 256, 12
+    width = 40
+    ids = rng.integers(-1, W * B * width + 3 * W * B, size=(T, k)).astype(np.int32)
+    table = np.tile(np.arange(width, dtype=np.int32), (3, 1))
+    req = rng.integers(0, 3, size=T).astype(np.int32)
+    for rank in range(W):
+        rows, valid, status = oracle.emit_rows(ids, W, rank, req, table, B, B)
+        assert status == 0
+        for t in range(T):
+            want = [g // W for g in ids[t].tolist()
+                    if g >= 0 and g % W == rank and g // W // B < width]
+            assert valid[t] == len(want)
+            assert rows[t, :len(want)].tolist() == want
+            assert np.all(rows[t, len(want):] == -1)
+
+
+def test_emit_rows_ranks_partition_the_selection():
+    """Over all ranks every selected id in the table's range is emitted
+    exactly once, and dropped blocks by none."""
+    lg, _, _ = inputs.decode_merge(W=4, rows=6, S=3000, n=64, k=256, skew_count=0, seed=9)
+    bits = lg.view(torch.int16).numpy().view(np.uint16).reshape(24, 3000)
+    packed = oracle.dcp_pack(bits, oracle.topk_rows(bits, 64)).reshape(4, 6, 66)
+    ids, _, _ = oracle.merge_packed(packed, 256)
+    W, B, width = 4, 16, 40  # local < 3000 -> blocks up to 187; half dropped
+    table = (np.arange(6 * width, dtype=np.int32).reshape(6, width) * 3 + 1)
+    req = np.arange(6, dtype=np.int32)[::-1].copy()
+    total = np.zeros(6, dtype=np.int64)
+    for rank in range(W):
+        rows, valid, _ = oracle.emit_rows(ids, W, rank, req, table, B, 2 * B)
+        total += valid
+        for t in range(6):
+            got = rows[t, :valid[t]]
+            assert len(set(got.tolist())) == len(got)  # distinct tokens, distinct rows
+    in_range = ((ids >= 0) & ((ids // W) // B < width)).sum(axis=1)
+    assert total.tolist() == in_range.tolist()
+    assert 0 < in_range.sum() < (ids >= 0).sum()
+
+
+def test_emit_rows_max_blocks_and_bad_requests():
+    ids = np.array([[1, 5, 9, 13, 17]], dtype=np.int32)  # rank 1 of W=4: locals 0..4
+    table = np.array([[10, 20, 30]], dtype=np.int32)
+    rows, valid, status = oracle.emit_rows(ids, 4, 1, np.array([0], np.int32), table, 2, 100,
+                                           max_blocks=2)
+    assert rows[0].tolist() == [1000, 1001, 2000, 2001, -1] and valid[0] == 4 and status == 0
+    rows, valid, status = oracle.emit_rows(ids, 4, 1, np.array([-1], np.int32), table, 2, 100)
+    assert rows[0].tolist() == [-1] * 5 and valid[0] == 0 and status == 4
