@@ -278,6 +278,14 @@ def _stage_decode(dev, flush, peak, satk):
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     recv = torch.zeros(satk.rescue_recv_words(T, n, k), dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # rank 0's physical KV rows: 64-token blocks, a permuted block table
+    B = 64
+    width = (S + B - 1) // B
+    g = torch.Generator(device=dev).manual_seed(1238)
+    table = torch.randperm(T * width, generator=g, device=dev).to(torch.int32).view(T, width)
+    req = torch.randperm(T, generator=g, device=dev).to(torch.int32)
+    rows_out = torch.empty((T, k), dtype=torch.int32, device=dev)
+    valid = torch.empty(T, dtype=torch.int32, device=dev)
     parts = {
         "local_topN": lambda: satk.topk_rows(flat, n, out=local),
         "pack": lambda: satk.dcp_pack(flat, local, out=packed.view(W * T, -1)),
@@ -285,6 +293,8 @@ def _stage_decode(dev, flush, peak, satk):
                                                       sat_word=sat, status=status),
         "rescue": lambda: satk.dcp_rescue_select(packed, lg, sat, ids, k, recv=recv,
                                                  status=status),
+        "emit_rows": lambda: satk.dcp_emit_rows(ids, W, 0, req, table, B, B, rows_out=rows_out,
+                                                valid_out=valid),
     }
     dec = {}
     for name, f in parts.items():

@@ -60,6 +60,9 @@ enum satk_rc {
                                         DCPTopkSelectKernel] */
 #define SATK_STATUS_DUPLICATE_KEYS 2 /* a repeated (score, id) candidate sat
                                         on the cut: fewer than K ids kept   */
+#define SATK_STATUS_BAD_REQUEST 4    /* satk_dcp_emit_rows: a req_id outside
+                                        the block table; that row emits
+                                        nothing                             */
 
 /* Largest K of satk_topk_rows and of the rescue push. */
 #define SATK_TOPK_MAX_K 4096
@@ -219,6 +222,45 @@ int satk_dcp_rescue_select_noalloc(const int32_t *packed, int32_t W, int64_t T,
                                    int64_t ld_out, int32_t *status,
                                    satk_stream_t stream);
 
+/*
+ * satk_dcp_emit_rows -- this rank's physical KV rows of the selected tokens
+ * [P2 DCPTopkSelectKernel docstring (emit_rows), dcp_topk_merge_rows].
+ *
+ * ids         : int32 [T, ld_ids], columns [0, k): the selected global ids
+ *               of each row (as written by satk_dcp_merge_select or
+ *               satk_dcp_rescue_select; -1 entries are skipped).
+ * W, dcp_rank : ranks, and this rank (0 <= dcp_rank < W).  A global id g
+ *               belongs to rank g % W; its local index is l = g / W.
+ * req_id      : int32 [T], the request of each row: its row of block_table.
+ * block_table : int32 [table_rows, ld_block_table], physical block ids of
+ *               each request; max_blocks (<= ld_block_table) is the table's
+ *               width: a token in block b = l / block_size >= max_blocks is
+ *               dropped.
+ * stride_rows : physical rows per block id.  The row of token l is
+ *               block_table[req_id[t], b] * stride_rows + l % block_size,
+ *               stored as the low 32 bits (the page computes it in 32-bit
+ *               integers).
+ * rows_out    : int32 [T, ld_rows_out], ld_rows_out >= k: the rows of this
+ *               rank's tokens in the order of their ids, then -1 up to k.
+ *               Columns [k, ld_rows_out) are never written.
+ * valid_out   : int32 [T], the number of rows emitted.
+ * A req_id outside [0, table_rows) emits nothing for its row and raises
+ * SATK_STATUS_BAD_REQUEST.
+ * Errors      : SATK_EINVAL for NULL ids/req_id/block_table/rows_out/
+ *               valid_out, T < 0, k < 1, ld_ids < k, W < 1, dcp_rank outside
+ *               [0, W), table_rows < 0, max_blocks < 0,
+ *               ld_block_table < max_blocks, block_size < 1,
+ *               ld_rows_out < k, T >= 2**31.
+ */
+int satk_dcp_emit_rows(const int32_t *ids, int64_t T, int32_t k, int64_t ld_ids,
+                       int32_t W, int32_t dcp_rank, const int32_t *req_id,
+                       const int32_t *block_table, int64_t table_rows,
+                       int64_t ld_block_table, int32_t max_blocks,
+                       int32_t block_size, int64_t stride_rows,
+                       int32_t *rows_out, int64_t ld_rows_out,
+                       int32_t *valid_out, int32_t *status,
+                       satk_stream_t stream);
+
 /* A static, human-readable string for an SATK_* return code. */
 const char *satk_status_string(int rc);
 
@@ -239,6 +281,13 @@ int dcp_rescue_select(const int32_t *packed, int32_t W, int64_t T, int32_t n,
                       const int32_t *sat_word, int32_t *recv,
                       int32_t *ids_out, int64_t ld_out, int32_t *status,
                       satk_stream_t stream);
+int dcp_emit_rows(const int32_t *ids, int64_t T, int32_t k, int64_t ld_ids,
+                  int32_t W, int32_t dcp_rank, const int32_t *req_id,
+                  const int32_t *block_table, int64_t table_rows,
+                  int64_t ld_block_table, int32_t max_blocks,
+                  int32_t block_size, int64_t stride_rows, int32_t *rows_out,
+                  int64_t ld_rows_out, int32_t *valid_out, int32_t *status,
+                  satk_stream_t stream);
 
 #ifdef __cplusplus
 }

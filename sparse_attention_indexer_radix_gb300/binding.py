@@ -21,12 +21,14 @@ SATK_F32, SATK_BF16 = 0, 1
 SATK_PAIRS_F32, SATK_PACKED_BF16 = 0, 1
 STATUS_SLOTS_EXCEEDED = 1
 STATUS_DUPLICATE_KEYS = 2
+STATUS_BAD_REQUEST = 4
 TOPK_MAX_K = 4096
 MERGE_MAX_CANDIDATES = 32768
 
 EXPORTS = ("satk_topk_rows", "satk_dcp_pack", "satk_dcp_merge_select",
            "satk_dcp_rescue_select", "satk_rescue_recv_words", "satk_status_string",
-           "topk_rows", "dcp_pack", "dcp_merge_select", "dcp_rescue_select")
+           "satk_dcp_emit_rows", "topk_rows", "dcp_pack", "dcp_merge_select",
+           "dcp_rescue_select", "dcp_emit_rows")
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +55,8 @@ def lib() -> ctypes.CDLL:
                 "satk_dcp_merge_select": [vp, c_int, i32, i64, i32, i32, vp, i64, vp, vp, vp],
                 "satk_dcp_rescue_select": [vp, i32, i64, i32, i32, vp, i64, i64, vp, vp, vp, vp,
                                            i64, vp, vp],
+                "satk_dcp_emit_rows": [vp, i64, i32, i64, i32, i32, vp, vp, i64, i64, i32, i32,
+                                       i64, vp, i64, vp, vp, vp],
             }
             for name, args in sigs.items():
                 f = getattr(L, name)
@@ -237,3 +241,45 @@ def dcp_rescue_select(packed: torch.Tensor, logits: torch.Tensor, sat_word: torc
                                       _stream(packed.device))
     _check(rc, "satk_dcp_rescue_select")
     return recv
+
+
+def dcp_emit_rows(ids: torch.Tensor, W: int, dcp_rank: int, req_id: torch.Tensor,
+                  block_table: torch.Tensor, block_size: int, stride_rows: int, *,
+                  k: int | None = None, max_blocks: int | None = None,
+                  rows_out: torch.Tensor | None = None,
+                  valid_out: torch.Tensor | None = None,
+                  status: torch.Tensor | None = None):
+    """This rank's physical KV rows of the selected global ids ``ids``
+    ([T, >= k] int32, as a merge writes them): ``block_table`` is int32
+    [R, width] (unit column stride; ``max_blocks`` defaults to its width),
+    ``req_id`` int32 [T].  Returns (rows_out [T, >= k] int32, valid_out [T]
+    int32)."""
+    _need_cuda(ids, req_id, block_table, rows_out, valid_out, status)
+    _rowmajor_2d(ids, "ids")
+    _rowmajor_2d(block_table, "block_table")
+    if ids.dtype != torch.int32 or req_id.dtype != torch.int32 or block_table.dtype != torch.int32:
+        raise SatkError("ids, req_id and block_table must be int32")
+    T = ids.shape[0]
+    k = ids.shape[1] if k is None else k
+    if not req_id.is_contiguous() or req_id.numel() < T:
+        raise SatkError("req_id must be contiguous int32 with T entries")
+    R, width = block_table.shape
+    max_blocks = width if max_blocks is None else max_blocks
+    if rows_out is None:
+        rows_out = torch.empty((T, k), dtype=torch.int32, device=ids.device)
+    if valid_out is None:
+        valid_out = torch.empty(T, dtype=torch.int32, device=ids.device)
+    _rowmajor_2d(rows_out, "rows_out")
+    if rows_out.dtype != torch.int32 or rows_out.shape[0] != T or rows_out.shape[1] < k:
+        raise SatkError(f"rows_out must be int32 [{T}, >= {k}]")
+    if valid_out.dtype != torch.int32 or not valid_out.is_contiguous() or valid_out.numel() < T:
+        raise SatkError("valid_out must be contiguous int32 with T entries")
+    ld_ids = ids.stride(0) if T > 1 else ids.shape[1]
+    ld_rows = rows_out.stride(0) if T > 1 else rows_out.shape[1]
+    ld_table = block_table.stride(0) if R > 1 else max(width, 1)
+    rc = lib().satk_dcp_emit_rows(_ptr(ids), T, k, ld_ids, W, dcp_rank, _ptr(req_id),
+                                  _ptr(block_table), R, ld_table, max_blocks, block_size,
+                                  stride_rows, _ptr(rows_out), ld_rows, _ptr(valid_out),
+                                  _ptr(status), _stream(ids.device))
+    _check(rc, "satk_dcp_emit_rows")
+    return rows_out, valid_out

@@ -150,3 +150,29 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros((2, 8))
     with pytest.raises(binding.SatkError):
         binding.topk_rows(x, 2)
+
+
+@no_gpu
+def test_emit_rows_rejects(lib):
+    f = lib.satk_dcp_emit_rows
+    ok = dict(ids=P, T=4, k=64, ld=64, W=8, rank=3, req=P, table=P, R=2, ldt=16, maxb=16,
+              B=64, stride=64, rows=P, ldr=64, valid=P, st=NULL)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["ids"], a["T"], a["k"], a["ld"], a["W"], a["rank"], a["req"], a["table"],
+                 a["R"], a["ldt"], a["maxb"], a["B"], a["stride"], a["rows"], a["ldr"],
+                 a["valid"], a["st"], NULL)
+    for name in ("ids", "req", "table", "rows", "valid"):
+        assert call(**{name: NULL}) == EINVAL
+    assert call(T=-1) == EINVAL
+    assert call(k=0) == EINVAL
+    assert call(ld=63) == EINVAL
+    assert call(W=0) == EINVAL
+    assert call(rank=8) == EINVAL
+    assert call(rank=-1) == EINVAL
+    assert call(R=-1) == EINVAL
+    assert call(maxb=17) == EINVAL    # wider than the table's row stride
+    assert call(B=0) == EINVAL
+    assert call(ldr=63) == EINVAL
+    assert call(T=0) == 0             # nothing to do, nothing launched

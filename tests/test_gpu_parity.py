@@ -396,3 +396,76 @@ def test_abi_rejects_with_real_buffers():
     assert L.satk_dcp_merge_select(p(out), 0, 1, 1, 48, 8, p(out), 8, None, None, None) == -1
     torch.cuda.synchronize()
     assert np.all(out.cpu().numpy() == 0)  # nothing was launched
+
+
+# ------------------------------------------------------------- emit_rows --
+
+def run_emit_rows(ids, W, rank, req, table, B, stride, max_blocks=None, ld_rows=None):
+    """GPU (through the C ABI) and oracle outputs for host int32 arrays."""
+    T, k = ids.shape
+    ld_rows = k if ld_rows is None else ld_rows
+    rows = torch.full((T, ld_rows), CANARY, dtype=torch.int32, device=DEV)
+    valid = torch.full((T,), CANARY, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    satk.dcp_emit_rows(torch.from_numpy(ids).to(DEV), W, rank, torch.from_numpy(req).to(DEV),
+                       torch.from_numpy(table).to(DEV), B, stride, max_blocks=max_blocks,
+                       rows_out=rows[:, :k] if ld_rows != k else rows, valid_out=valid,
+                       status=st)
+    want_rows, want_valid, want_st = oracle.emit_rows(ids, W, rank, req, table, B, stride,
+                                                      max_blocks=max_blocks, ld_rows=ld_rows)
+    return (rows.cpu().numpy(), valid.cpu().numpy(), int(st.item())), \
+        (want_rows, want_valid, want_st)
+
+
+def test_emit_rows_hand_worked_example_on_gpu():
+    import test_oracle_pins as pins
+    g = pins._emit_rows_golden()
+    got, want = run_emit_rows(np.array(g["ids"], np.int32), g["W"], g["rank"],
+                              np.array(g["req"], np.int32), np.array(g["table"], np.int32),
+                              g["block_size"], g["stride_rows"], ld_rows=10)
+    assert got[0][:, :8].tolist() == g["rows"]
+    assert np.all(got[0][:, 8:] == CANARY)
+    assert got[1].tolist() == g["valid"] and got[2] == g["status"]
+
+
+@pytest.mark.parametrize("k,ld_rows", [(2048, 2048), (64, 70), (13, 13), (5000, 5003)])
+def test_emit_rows_matches_oracle(k, ld_rows):
+    rng = np.random.default_rng(k)
+    T, W, B, width, R = 37, 8, 64, 50, 5
+    ids = rng.integers(-3, W * B * width * 5 // 4, size=(T, k)).astype(np.int32)
+    ids[3] = -1                                     # an empty row
+    table = rng.integers(0, 1 << 20, size=(R, width)).astype(np.int32)
+    table[1, 7] = 40_000_000                        # wraps at stride 64
+    req = rng.integers(0, R, size=T).astype(np.int32)
+    req[5], req[6] = -1, R                          # bad requests
+    for rank in (0, 3, 7):
+        for max_blocks in (None, 0, 17):
+            got, want = run_emit_rows(ids, W, rank, req, table, B, 64, max_blocks=max_blocks,
+                                      ld_rows=ld_rows)
+            assert_rows_equal(got[0], want[0], f"emit_rows k={k} rank={rank} mb={max_blocks}")
+            assert np.array_equal(got[1], want[1]) and got[2] == want[2] == 4
+
+
+def test_emit_rows_after_the_decode_merge():
+    """The decode pipeline's final ids (merge and rescue) to each rank's rows."""
+    W, T, S, n, k = 8, 32, 20000, 128, 1024
+    lg, _, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, skew_count=300, seed=21,
+                                   device=DEV)
+    local = satk.topk_rows(lg.view(W * T, S), n)
+    packed = satk.dcp_pack(lg.view(W * T, S), local).view(W, T, n + n // 32)
+    sat = torch.zeros(T, dtype=torch.int32, device=DEV)
+    ids = satk.dcp_merge_select(packed, k, packed=True, sat_word=sat)
+    satk.dcp_rescue_select(packed, lg, sat, ids, k)
+    B = 64
+    width = (S + B - 1) // B
+    rng = np.random.default_rng(5)
+    table = rng.permutation(T * width).astype(np.int32).reshape(T, width)
+    req = rng.permutation(T).astype(np.int32)
+    ids_h = ids.cpu().numpy()
+    total = np.zeros(T, dtype=np.int64)
+    for rank in range(W):
+        got, want = run_emit_rows(ids_h, W, rank, req, table, B, B)
+        assert_rows_equal(got[0], want[0], f"decode emit_rows rank={rank}")
+        assert np.array_equal(got[1], want[1]) and got[2] == 0
+        total += got[1]
+    assert np.array_equal(total, (ids_h >= 0).sum(axis=1))  # every token owned once
