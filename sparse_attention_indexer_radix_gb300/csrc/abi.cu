@@ -1,5 +1,33 @@
-// abi.cu -- status strings and the short-name aliases of the C ABI.
+// abi.cu -- status strings, the short-name aliases of the C ABI, and the
+// host helpers that keep state (the resident-CTA cache).
+#include <mutex>
+#include <unordered_map>
+
 #include "satk_host.hpp"
+
+namespace satk {
+
+int64_t resident_ctas(const void *kernel, int block, size_t smem) {
+  static std::mutex mu;
+  static std::unordered_map<const void *, int64_t> cache[64];  // per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache[dev].find(kernel);
+    if (it != cache[dev].end()) return it->second;
+  }
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem) != cudaSuccess)
+    return 0;
+  const int64_t n = static_cast<int64_t>(sms) * (per_sm < 1 ? 1 : per_sm);
+  std::lock_guard<std::mutex> g(mu);
+  cache[dev][kernel] = n;
+  return n;
+}
+
+}  // namespace satk
 
 extern "C" const char *satk_status_string(int rc) {
   switch (rc) {

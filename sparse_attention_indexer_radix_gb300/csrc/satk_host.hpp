@@ -27,4 +27,9 @@ inline bool allow_smem(K kernel, size_t bytes) {
                               static_cast<int>(bytes)) == cudaSuccess;
 }
 
+// CTAs of `kernel` (block threads, smem dynamic bytes) the current device
+// holds at once: SMs x resident CTAs per SM, computed once per kernel and
+// device.  0 on error.
+int64_t resident_ctas(const void *kernel, int block, size_t smem);
+
 }  // namespace satk

@@ -78,21 +78,17 @@ __device__ __forceinline__ uint32_t vec_raw(const uint4 &v, int s) {
 
 // ------------------------------------------------------------ threshold --
 
-// Samples BLOCK*SPT columns of the row -- BLOCK*SPT/32 runs of 32
+// Loads the sample of a row: BLOCK*SPT columns in BLOCK*SPT/32 runs of 32
 // consecutive columns spread evenly over [0, end), one coalesced load per
-// warp and run, so the sample touches few memory sectors -- and returns a
-// key T0 with P(fewer than K columns of the row have key >= T0) negligible
-// under random sampling: T0 is the sample's r-th largest key,
-// r = mu + 4 sqrt(mu) + 4 with mu = K * samples / end.  Returns 1 (every
-// valid column) when the sample holds fewer than r valid keys.  Needs
-// end >= 32 * BLOCK * SPT / 32.
+// warp and run, so the sample touches few memory sectors.  Their keys go to
+// the first 32*SPT entries of each warp's list segment.  Needs
+// end >= BLOCK * SPT.
 template <typename T, int BLOCK, int SPT, int SUB>
-__device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
-                                     ListSmem<BLOCK, SUB> &sm) {
+__device__ __forceinline__ Seg sample_keys(const T *__restrict__ xr, int end,
+                                           ListSmem<BLOCK, SUB> &sm) {
   static_assert(SPT * 32 <= SUB, "samples must fit a warp segment");
-  constexpr int S = BLOCK * SPT;
+  constexpr int NRUNS = BLOCK * SPT / 32;
   const int lane = lane_id(), warp = warp_id();
-  constexpr int NRUNS = S / 32;
   uint32_t raw[SPT];
 #pragma unroll
   for (int q = 0; q < SPT; ++q) {
@@ -102,11 +98,28 @@ __device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
   }
 #pragma unroll
   for (int q = 0; q < SPT; ++q) sm.key[warp * SUB + q * 32 + lane] = key_of_raw<T>(raw[q]);
-  const float mu = static_cast<float>(K) * S / static_cast<float>(end);
-  int r = static_cast<int>(ceilf(mu + 4.f * sqrtf(mu) + 4.f));
-  r = r < 1 ? 1 : (r > S ? S : r);
   __syncwarp();
-  const Seg sg{warp * SUB, 32 * SPT};
+  return Seg{warp * SUB, 32 * SPT};
+}
+
+// The rank r of the sample's key that is T0: with mu = K * samples / end
+// columns of the top K expected in the sample, r = mu + 4 sqrt(mu) + 4 makes
+// P(fewer than K columns of the row have key >= T0) negligible under random
+// sampling.
+__device__ __forceinline__ int sample_rank(int K, int samples, int end) {
+  const float mu = static_cast<float>(K) * samples / static_cast<float>(end);
+  const int r = static_cast<int>(ceilf(mu + 4.f * sqrtf(mu) + 4.f));
+  return r < 1 ? 1 : (r > samples ? samples : r);
+}
+
+// T0 of a row: the r-th largest key of its sample (sample_keys,
+// sample_rank); 1 (every valid column) when the sample holds fewer than r
+// valid keys.
+template <typename T, int BLOCK, int SPT, int SUB>
+__device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
+                                     ListSmem<BLOCK, SUB> &sm) {
+  const Seg sg = sample_keys<T, BLOCK, SPT, SUB>(xr, end, sm);
+  const int r = sample_rank(K, BLOCK * SPT, end);
   const Sel s = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, r, sm.sel, 3);
   return s.take_all ? 1u : s.T;
 }
@@ -235,6 +248,20 @@ __device__ __forceinline__ void prefetch_groups(const T *__restrict__ xr, int ga
       }
     }
   }
+}
+
+// Groups per lane per batch of the filtered pass, and samples per thread of
+// the threshold step.
+constexpr int kRowBatch = 4;
+constexpr int kRowSample = 4;
+
+// L2 prefetch of the first two batches of every warp's stretch of a row of
+// `end` columns: what the filtered pass reads first.
+template <typename T, int BLOCK, int ALIGN>
+__device__ __forceinline__ void prefetch_row_head(const T *__restrict__ xr, int end) {
+  int g0, g1;
+  warp_stretch<BLOCK>(end, g0, g1);
+  prefetch_groups<T, ALIGN>(xr, g0, min(g1, g0 + 2 * 32 * kRowBatch));
 }
 
 // Every warp streams its own contiguous stretch of 8-element groups (one
@@ -547,18 +574,15 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   constexpr int KB = KeyOf<T>::kBits;
   constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
   constexpr bool VECLOAD = ALIGN != 0;
-  constexpr int U = 4;  // groups per lane per batch of the filtered pass
+  constexpr int U = kRowBatch;
   const bool all = end <= CAP;
-  {  // start the copy engine on the first batches of this warp's stretch
-    int g0, g1;
-    warp_stretch<BLOCK>(end, g0, g1);
-    prefetch_groups<T, ALIGN>(xr, g0, min(g1, g0 + 2 * 32 * U));
-  }
+  // start the copy engine on the first batches of this warp's stretch
+  prefetch_row_head<T, BLOCK, ALIGN>(xr, end);
   float t0f;
   if (all) {
     t0f = __uint_as_float(0xff800000u);  // -inf: every valid column
   } else {
-    t0f = threshold_float<KB>(sample_threshold<T, BLOCK, 4, SUB>(xr, end, K, sm));
+    t0f = threshold_float<KB>(sample_threshold<T, BLOCK, kRowSample, SUB>(xr, end, K, sm));
   }
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear

@@ -11,6 +11,7 @@
 #include <cmath>
 
 #include "satk_host.hpp"
+#include "satk_cluster.cuh"
 #include "satk_rows.cuh"
 #include "satk_warp.cuh"
 
@@ -106,6 +107,81 @@ inline bool warp_rows_fit(int cols, int K) {
   return list + 4.0 * list / std::sqrt(r) <= kWarpList;
 }
 
+// Few long rows: a cluster of C CTAs per row (satk_cluster.cuh); the grid
+// is rows x C, CTA blockIdx.x % C of the cluster taking slice
+// blockIdx.x % C of row blockIdx.x / C.
+template <typename T, int BLOCK, int SUB, int ALIGN, int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(BLOCK, 1024 / BLOCK)
+    topk_rows_cluster_kernel(const T *__restrict__ x, int64_t ld, int cols,
+                             const int32_t *__restrict__ row_ends, int K,
+                             int32_t *__restrict__ out, int64_t ld_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &cs = *reinterpret_cast<ClusterSmem<BLOCK, SUB> *>(smem_raw);
+  cg::cluster_group cl = cg::this_cluster();
+  const int64_t row = blockIdx.x / C;
+  zero_hist(cs.ls.sel);
+  __syncthreads();
+  cluster_topk_row<T, BLOCK, SUB, ALIGN, C>(cl, x + row * ld, row_end_of(row_ends, row, cols), K,
+                                            out + row * ld_out, cs);
+}
+
+template <typename T, int BLOCK, int SUB, int ALIGN, int C>
+int launch_cluster(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
+                   int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_cluster_kernel<T, BLOCK, SUB, ALIGN, C>;
+  const size_t smem = sizeof(ClusterSmem<BLOCK, SUB>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(rows * C)), BLOCK, smem, st>>>(x, ld, cols, row_ends, K,
+                                                                   out, ld_out);
+  return launch_status();
+}
+
+// Cluster size for `rows` rows when one CTA per row would fill fewer than
+// three waves of resident CTAs (0: no cluster): the smallest of 2, 4, 8
+// that reaches three waves, else 8.  A cluster adds barriers to every step
+// of a row, which only pays when the slices stay long: with at least one
+// full wave of rows, a slice under kClusterMinSlice bytes keeps one CTA per
+// row (measured: 1024 bf16 rows of 128 KB ran 2x slower on two-CTA
+// clusters, 1310 fp32 rows of 400 KB 1.35x faster, 256 bf16 rows of up to
+// 256 KB 3.2x faster on eight).
+constexpr int64_t kClusterMinSlice = 128 * 1024;
+
+template <typename T, int BLOCK, int SUB, int ALIGN>
+int cluster_size(int64_t rows, int cols) {
+  if (rows > INT32_MAX / 8 || cols < 8 * 2 * ListSmem<BLOCK, SUB>::CAP) return 0;
+  const int64_t resident =
+      resident_ctas(reinterpret_cast<const void *>(topk_rows_kernel<T, BLOCK, SUB, ALIGN>),
+                    BLOCK, sizeof(ListSmem<BLOCK, SUB>));
+  if (resident <= 0 || rows >= 3 * resident) return 0;
+  int c = 8;
+  for (int t = 2; t < 8; t *= 2)
+    if (rows * t >= 3 * resident) {
+      c = t;
+      break;
+    }
+  const int64_t slice = static_cast<int64_t>(cols) * static_cast<int64_t>(sizeof(T)) / c;
+  if (rows >= resident && slice < kClusterMinSlice) return 0;
+  return c;
+}
+
+template <typename T, int BLOCK, int SUB, int ALIGN>
+int launch_rows_cta(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
+                    int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  switch (cluster_size<T, BLOCK, SUB, ALIGN>(rows, cols)) {
+    case 2:
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 2>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                     st);
+    case 4:
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 4>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                     st);
+    case 8:
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 8>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                     st);
+    default:
+      return launch<T, BLOCK, SUB, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  }
+}
+
 // The list holds (BLOCK/32) warps x SUB candidates.
 template <typename T, int ALIGN>
 int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
@@ -115,8 +191,10 @@ int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *r
   if (cols <= kShortCols && K <= 512)
     return launch<T, kShortBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
   if (K <= 1024)
-    return launch<T, kBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
-  return launch<T, kBlock, 1024, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+    return launch_rows_cta<T, kBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                  st);
+  return launch_rows_cta<T, kBlock, 1024, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                 st);
 }
 
 // Widest load every row start allows: 32 or 16 bytes, else element loads.

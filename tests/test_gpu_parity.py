@@ -143,6 +143,43 @@ def test_topk_warp_rows_edges(dtype, ld):
         assert_rows_equal(got, want, f"warp rows {dtype} ld={ld} k={k}")
 
 
+@pytest.mark.parametrize("rows,dtype,ld", [(8, torch.float32, 70000), (600, torch.float32, 70000),
+                                           (1000, torch.float32, 70004),
+                                           (600, torch.bfloat16, 70001)])
+def test_topk_few_long_rows(rows, dtype, ld):
+    """Few long rows (a cluster of CTAs per row: 8, 600 and 1000 rows take
+    different cluster sizes): random row ends around the slice and list
+    sizes, NaN, constant and few-level rows (the exact path), fp32 and bf16,
+    aligned and unaligned rows; sampled rows against the oracle."""
+    cols = 70000
+    x, _ = inputs.prefill(rows=rows, cols=cols, seed=rows + ld, dtype=torch.float32)
+    g = torch.Generator().manual_seed(rows)
+    ends = torch.randint(0, cols + 1, (rows,), generator=g, dtype=torch.int32)
+    special = {0: 0, 1: cols, 2: 4000, 3: 16352, 4: 16353, 5: 32704, 6: 32705, 7: 65535}
+    for r, e in special.items():
+        ends[r] = e
+    x[1] = float("nan")
+    x[2, ::2] = float("nan")
+    if rows > 8:
+        for r, e in enumerate((8176, 8177, 16368, 16369, 32736, 65472, 65473), start=11):
+            ends[r] = e                                       # list-size boundaries
+        x[8] = 0.5                                            # one value
+        x[9] = torch.randint(0, 4, (cols,), generator=g).float()  # four levels
+        x[10, 100:700] = 9.0                                  # a clustered tied top block
+    x = x.to(dtype)
+    sample = sorted(set(range(min(rows, 18))) |
+                    set(np.random.default_rng(rows).integers(0, rows, 24).tolist()))
+    buf = torch.zeros((rows, ld), dtype=dtype, device=DEV)
+    buf[:, :cols] = x.to(DEV)
+    for k in (1, 512, 2048):
+        out = torch.full((rows, k + 3), CANARY, dtype=torch.int32, device=DEV)
+        satk.topk_rows(buf[:, :cols], k, row_ends=ends.to(DEV), out=out)
+        got = out.cpu().numpy()[sample]
+        want = np.full((len(sample), k + 3), CANARY, dtype=np.int32)
+        oracle.topk_rows(host_view(x[sample]), k, row_ends=ends[sample].numpy(), out=want)
+        assert_rows_equal(got, want, f"few long rows={rows} {dtype} k={k}")
+
+
 @pytest.mark.parametrize("mode", ["plus100", "times1e-8"])
 def test_topk_concentrated_distributions(mode):
     x, ends = inputs.prefill_shifted(64, 8192, mode)
