@@ -355,6 +355,18 @@ def _stage_robust(dev, flush, peak, satk):
         x, ends = inputs.prefill_shifted(8192, 8192, mode, device=dev)
         one(f"dist_{mode}_8192x8192_f32_K512", x, ends)
         del x
+    # decode-shaped few long rows (the DCP kernels page: the cluster variant
+    # of its selector for <= 6 rows at >= 512K columns): bf16, K = 384
+    x, ends = inputs.prefill(rows=4, cols=524288, seed=1260, device=dev, causal=False,
+                             dtype=torch.bfloat16)
+    out = torch.empty((4, 384), dtype=torch.int32, device=dev)
+    fn = lambda: satk.topk_rows(x, 384, row_ends=ends, out=out)  # noqa: E731
+    for _ in range(3):
+        fn()
+    ms = timed_calls(fn, 10, flush)
+    nb = 4 * 524288 * 2 + 4 * 384 * 4
+    st["few_rows_4x524288_bf16_K384"] = {"us": ms * 1e3, "gbs": nb / (ms * 1e-3) / 1e9,
+                                         "frac": nb / (ms * 1e-3) / 1e9 / peak}
     return st
 
 

@@ -180,6 +180,16 @@ def test_topk_few_long_rows(rows, dtype, ld):
         assert_rows_equal(got, want, f"few long rows={rows} {dtype} k={k}")
 
 
+def test_topk_decode_shaped_few_rows():
+    """A handful of very long bf16 rows (the benchmark's 4 x 524288 case and
+    shorter row ends), K = 384 and 2048."""
+    x, _ = inputs.prefill(rows=5, cols=524288, seed=1260, causal=False, dtype=torch.bfloat16)
+    ends = torch.tensor([524288, 524287, 300001, 70000, 5], dtype=torch.int32)
+    for k in (384, 2048):
+        got, want = run_topk(x, k, ends, k)
+        assert_rows_equal(got, want, f"few rows k={k}")
+
+
 @pytest.mark.parametrize("mode", ["plus100", "times1e-8"])
 def test_topk_concentrated_distributions(mode):
     x, ends = inputs.prefill_shifted(64, 8192, mode)
