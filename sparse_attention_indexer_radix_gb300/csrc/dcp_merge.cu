@@ -396,6 +396,22 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
     tie2 = s2.tie;
   }
   int32_t *out = ids + t * ld_out;
+  if (!use2) {  // block-uniform: no tie at the K-th score (the usual case)
+    const bool all_keys = s1.take_all;
+    const uint32_t T1 = s1.T;
+    const int n1 = list_emit1<BLOCK>(
+        [&](int i) {
+          const uint32_t k = sm.key[i];
+          return k != 0u && (all_keys || k >= T1);
+        },
+        sg,
+        [&](int rank, int i) {
+          if ((unsigned)rank < (unsigned)K) out[rank] = static_cast<int32_t>(sm.val[i]);
+        },
+        sm.sel);
+    for (int q = max(0, n1) + (int)threadIdx.x; q < K; q += BLOCK) out[q] = -1;
+    return;
+  }
   const int2 tot = list_emit<BLOCK>(
       [&](int i) -> int {
         const uint32_t k = sm.key[i];

@@ -212,6 +212,38 @@ __device__ int2 list_emit(Cls cls, const Seg &sg, EmitA emitA, EmitB emitB, Sele
   return tot;
 }
 
+// list_emit with one group: sel(i) chooses absolute entry i; emit(rank, i)
+// receives each chosen entry's rank in list order.  Returns the count.
+// Two barriers.
+template <int BLOCK, class SelF, class Emit>
+__device__ int list_emit1(SelF sel, const Seg &sg, Emit emit, SelectSmem<BLOCK> &sm) {
+  static_assert(BLOCK / 32 * 32 <= 2048, "ballot store exceeds the histogram");
+  const int lane = lane_id();
+  const unsigned lt = (1u << lane) - 1u;
+  uint32_t *bal = sm.hist + warp_id() * 32;
+  const int R = sg.rounds();
+  int ca = 0;
+  for (int j = 0; j < R; ++j) {
+    const int i = j * 32 + lane;
+    const unsigned ba = __ballot_sync(kFull, i < sg.cnt && sel(sg.base + i));
+    if (lane == 0 && j < 32) bal[j] = ba;
+    ca += __popc(ba);
+  }
+  int total;
+  int ra = block_warp_prefix<BLOCK>(ca, sm.wtot[3], &total);
+  for (int j = 0; j < R; ++j) {
+    const int i = j * 32 + lane;
+    const unsigned ba =
+        j < 32 ? bal[j] : __ballot_sync(kFull, i < sg.cnt && sel(sg.base + i));
+    if ((ba >> lane) & 1u) emit(ra + __popc(ba & lt), sg.base + i);
+    ra += __popc(ba);
+  }
+  __syncwarp();
+  bal[lane] = 0u;
+  __syncthreads();
+  return total;
+}
+
 // Row top-K layout from the list: entries above the K-th key in list order,
 // then entries equal to it in list order up to K, then fill(pos) up to K.
 template <int BLOCK, int SUB, class Put, class Fill>
