@@ -224,13 +224,14 @@ __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &
   return r;
 }
 
-// Select over the union of the lists and the ordered emit into o[0, K):
-// entries above the K-th key in (CTA, list) order, then entries equal to it
-// up to K, then -1 when fewer than K in all.  col0 is this CTA's first
-// column (list values are slice-relative).
-template <int BLOCK, int SUB, int C>
+// Select over the union of the lists and the ordered emit: put(pos, key,
+// col) for the entries above the K-th key in (CTA, list) order, then for
+// the entries equal to it up to K; fill(pos) for [n, K) when only n < K
+// candidates exist in all.  col0 is this CTA's first column (list values
+// are slice-relative).
+template <int BLOCK, int SUB, int C, class Put, class Fill>
 __device__ void cluster_topk_emit(cg::cluster_group &cl, ClusterSmem<BLOCK, SUB> &cs,
-                                  const Seg &sg, int K, int col0, int32_t *__restrict__ o,
+                                  const Seg &sg, int K, int col0, Put put, Fill fill,
                                   WarpStats pre) {
   ListSmem<BLOCK, SUB> &sm = cs.ls;
   const int crank = static_cast<int>(cl.block_rank());
@@ -305,11 +306,13 @@ __device__ void cluster_topk_emit(cg::cluster_group &cl, ClusterSmem<BLOCK, SUB>
     }
     if ((ba >> lane) & 1u) {
       const int pos = ra + __popc(ba & lt);
-      if ((unsigned)pos < (unsigned)K) o[pos] = static_cast<int32_t>(sm.val[sg.base + i]) + col0;
+      if ((unsigned)pos < (unsigned)K)
+        put(pos, sm.key[sg.base + i], static_cast<int>(sm.val[sg.base + i]) + col0);
     }
     if ((bb >> lane) & 1u) {
       const int pos = rb + __popc(bb & lt);
-      if ((unsigned)pos < (unsigned)K) o[pos] = static_cast<int32_t>(sm.val[sg.base + i]) + col0;
+      if ((unsigned)pos < (unsigned)K)
+        put(pos, sm.key[sg.base + i], static_cast<int>(sm.val[sg.base + i]) + col0);
     }
     ra += __popc(ba);
     rb += __popc(bb);
@@ -319,14 +322,16 @@ __device__ void cluster_topk_emit(cg::cluster_group &cl, ClusterSmem<BLOCK, SUB>
   bal[lane + 32] = 0u;
   __syncthreads();
   if (sel.take_all && crank == C - 1)
-    for (int q = totA + static_cast<int>(threadIdx.x); q < K; q += BLOCK) o[q] = -1;
+    for (int q = totA + static_cast<int>(threadIdx.x); q < K; q += BLOCK) fill(q);
 }
 
-// The whole row on a cluster of C CTAs (this CTA is rank cl.block_rank()).
-// The histogram must be zero on entry.
-template <typename T, int BLOCK, int SUB, int ALIGN, int C>
+// The whole row on a cluster of C CTAs (this CTA is rank cl.block_rank()):
+// put(pos, key, column) for output position pos of the row's top-K layout
+// (the layout of topk_row), fill(pos) for the positions past the last
+// candidate.  The histogram must be zero on entry.
+template <typename T, int BLOCK, int SUB, int ALIGN, int C, class Put, class Fill>
 __device__ void cluster_topk_row(cg::cluster_group &cl, const T *__restrict__ xr, int end,
-                                 int K, int32_t *__restrict__ o, ClusterSmem<BLOCK, SUB> &cs) {
+                                 int K, Put put, Fill fill, ClusterSmem<BLOCK, SUB> &cs) {
   constexpr int KB = KeyOf<T>::kBits;
   constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
   constexpr bool VECLOAD = ALIGN != 0;
@@ -370,16 +375,16 @@ __device__ void cluster_topk_row(cg::cluster_group &cl, const T *__restrict__ xr
     total += static_cast<int>(cluster_word(cl, &cs.pub[kPubCount], c));
   }
   if (!over && (all || total >= K)) {  // cluster-uniform
-    cluster_topk_emit<BLOCK, SUB, C>(cl, cs, sg, K, col0, o, st);
+    cluster_topk_emit<BLOCK, SUB, C>(cl, cs, sg, K, col0, put, fill, st);
   } else if (crank == 0) {  // the exact path, on CTA 0 over the whole row
     __syncthreads();
     sg = collect_exact<T, BLOCK, SUB, VECLOAD>(xr, end, K, sm);
     list_topk_emit<BLOCK, SUB>(
         sm, sg, K,
         [&](int pos, int i) {
-          if ((unsigned)pos < (unsigned)K) o[pos] = static_cast<int32_t>(sm.val[i]);
+          if ((unsigned)pos < (unsigned)K) put(pos, sm.key[i], static_cast<int>(sm.val[i]));
         },
-        [&](int pos) { o[pos] = -1; });
+        fill);
   }
   cl.sync();  // no CTA leaves while another may still read its shared memory
 }

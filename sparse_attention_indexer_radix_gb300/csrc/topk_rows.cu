@@ -121,8 +121,10 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(BLOCK, 1024 / BLOCK)
   const int64_t row = blockIdx.x / C;
   zero_hist(cs.ls.sel);
   __syncthreads();
-  cluster_topk_row<T, BLOCK, SUB, ALIGN, C>(cl, x + row * ld, row_end_of(row_ends, row, cols), K,
-                                            out + row * ld_out, cs);
+  int32_t *o = out + row * ld_out;
+  cluster_topk_row<T, BLOCK, SUB, ALIGN, C>(
+      cl, x + row * ld, row_end_of(row_ends, row, cols), K,
+      [&](int pos, uint32_t, int col) { o[pos] = col; }, [&](int pos) { o[pos] = -1; }, cs);
 }
 
 template <typename T, int BLOCK, int SUB, int ALIGN, int C>

@@ -387,6 +387,24 @@ def test_decode_merge_full_workload():
     packed_contract(got["packed"].reshape(W * T, -1), bits.reshape(W * T, S), None, n)
 
 
+@pytest.mark.parametrize("k", [512, 2048])
+def test_decode_merge_long_rank_rows(k):
+    """Rank rows long enough for the clustered push: row ends around the
+    cluster's slice and list sizes, a half-NaN rank row, a skewed rank."""
+    W, T, S, n = 4, 16, 40000, 128
+    lg, skewed, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, skew_count=400, seed=k)
+    bits = bits_of(lg)
+    bits[1, 3, 1::2] = 0xFFC3
+    lg = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    g = torch.Generator().manual_seed(k)
+    ends = torch.randint(S // 2, S + 50, (W, T), generator=g, dtype=torch.int32)
+    ends[:, 0] = torch.tensor([0, 10, 65472 // 8 * 8, S])[:W]
+    ends[:, 1] = torch.tensor([32704, 32705, 32736, 32737])[:W]
+    got = _decode_gpu(lg, n, k, row_ends=ends)
+    want = _decode_oracle(lg, n, k, row_ends=ends)
+    _compare_decode(got, want, f"decode long rank rows k={k}")
+
+
 def test_decode_merge_row_ends_nan_and_small():
     W, T, S, n, k = 4, 12, 3000, 64, 512
     lg, _, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, skew_count=120, seed=77)
