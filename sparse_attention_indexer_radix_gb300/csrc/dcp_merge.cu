@@ -383,52 +383,10 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   __syncwarp();
 
   // ---- select: by score, then by global id among ties with the K-th
-  const Sel s1 = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, K, sm.sel, 8,
-                                    ok ? st : stats_unknown());
-  uint32_t t2 = 0u;
-  bool use2 = false, tie2 = false;
-  if (!s1.take_all && s1.tie) {
-    const Sel s2 = list_select<BLOCK>(
-        [&](int i) { return sm.key[i] == s1.T ? 0xffffffffu - sm.val[i] : 0u; }, sg, s1.need,
-        sm.sel);
-    use2 = true;
-    t2 = s2.T;
-    tie2 = s2.tie;
-  }
   int32_t *out = ids + t * ld_out;
-  if (!use2) {  // block-uniform: no tie at the K-th score (the usual case)
-    const bool all_keys = s1.take_all;
-    const uint32_t T1 = s1.T;
-    const int n1 = list_emit1<BLOCK>(
-        [&](int i) {
-          const uint32_t k = sm.key[i];
-          return k != 0u && (all_keys || k >= T1);
-        },
-        sg,
-        [&](int rank, int i) {
-          if ((unsigned)rank < (unsigned)K) out[rank] = static_cast<int32_t>(sm.val[i]);
-        },
-        sm.sel);
-    for (int q = max(0, n1) + (int)threadIdx.x; q < K; q += BLOCK) out[q] = -1;
-    return;
-  }
-  const int2 tot = list_emit<BLOCK>(
-      [&](int i) -> int {
-        const uint32_t k = sm.key[i];
-        if (k == 0u) return 0;
-        if (s1.take_all) return 1;
-        if (!use2) return k >= s1.T ? 1 : 0;
-        if (k != s1.T) return k > s1.T ? 1 : 0;
-        const uint32_t k2 = 0xffffffffu - sm.val[i];
-        return (tie2 ? k2 > t2 : k2 >= t2) ? 1 : 0;
-      },
-      sg,
-      [&](int rank, int i, int2) {
-        if ((unsigned)rank < (unsigned)K) out[rank] = static_cast<int32_t>(sm.val[i]);
-      },
-      [](int, int, int2) {}, sm.sel);
-  for (int q = max(0, tot.x) + (int)threadIdx.x; q < K; q += BLOCK) out[q] = -1;
-  if (tie2 && status != nullptr && threadIdx.x == 0) atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
+  const bool dup = list_merge_emit<BLOCK, SUB>(
+      sm, sg, K, [&](int pos, int32_t v) { out[pos] = v; }, ok ? st : stats_unknown());
+  if (dup && status != nullptr && threadIdx.x == 0) atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
 }
 
 template <int SUB, int ALIGN>

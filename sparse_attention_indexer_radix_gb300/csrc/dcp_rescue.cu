@@ -97,25 +97,20 @@ struct RescueSmem {
   uint32_t gid[BLOCK * KPT];
 };
 
+// The register select over every candidate slot (KPT per thread): the
+// exact path when the filtered list of rescue_select_kernel overflows.
 template <int BLOCK, int KPT>
-__global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
-    const int32_t *__restrict__ packed, int W, int64_t T, int n, int K, int slots,
-    const int32_t *__restrict__ sat_word, const int32_t *__restrict__ recv,
-    int32_t *__restrict__ ids, int64_t ld_out, int32_t *__restrict__ status) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  auto &sm = *reinterpret_cast<RescueSmem<BLOCK, KPT> *>(smem_raw);
+__device__ void rescue_select_regs(RescueSmem<BLOCK, KPT> &sm, const int32_t *__restrict__ packed,
+                                   int W, int64_t T, int n, int K, int slots, uint32_t mask,
+                                   uint32_t tau, const int32_t *__restrict__ recv,
+                                   int32_t *__restrict__ out, int32_t *__restrict__ status) {
   const int64_t t = blockIdx.x;
-  const uint32_t sw = static_cast<uint32_t>(sat_word[t]);
-  const uint32_t mask = sw >> 16, tau = sw & 0xffffu;
-  if (mask == 0u) return;  // round 1 was exact
   const int nsat = __popc(mask);
-  if (nsat > slots || (mask >> W) != 0u) return;  // reported by the push
   const int lane = lane_id();
   const int r1 = W * n;
   const int total = r1 + slots * K;
   const int words_r1 = n + n / 32, words_k = K + K / 32;
   zero_hist(sm.sel);
-
   uint32_t keys[KPT];
 #pragma unroll
   for (int g = 0; g < KPT; ++g) {
@@ -146,7 +141,6 @@ __global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
     sm.gid[fb + lane] = gid;
   }
   __syncthreads();
-  int32_t *out = ids + t * ld_out;
   const MergeOut m = merge_core<BLOCK, KPT, 16>(
       keys, [&](int i) { return sm.gid[flat_pos<KPT, 1>(i)]; },
       [&](int pos, int32_t v) {
@@ -157,12 +151,105 @@ __global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
     atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
 }
 
+// One CTA per row; a zero mask costs one load.  The candidates at or above
+// tau16 -- the round-1 words of the ranks outside the mask, then the pushed
+// lists -- are filtered in flat order into the shared-memory list (each warp
+// over a contiguous stretch, 32 candidates per step), and the list merge
+// select picks K.  The round-1 choice (K candidates scoring >= tau16) is
+// among them, so no candidate below tau16 can be chosen.  A warp segment
+// that would overflow sends the row to the register select over every slot.
+template <int BLOCK, int KPT, int SUB>
+__global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
+    const int32_t *__restrict__ packed, int W, int64_t T, int n, int K, int slots,
+    const int32_t *__restrict__ sat_word, const int32_t *__restrict__ recv,
+    int32_t *__restrict__ ids, int64_t ld_out, int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &sm = *reinterpret_cast<ListSmem<BLOCK, SUB> *>(smem_raw);
+  constexpr int NW = BLOCK / 32;
+  const int64_t t = blockIdx.x;
+  const uint32_t sw = static_cast<uint32_t>(sat_word[t]);
+  const uint32_t mask = sw >> 16, tau = sw & 0xffffu;
+  if (mask == 0u) return;  // round 1 was exact
+  const int nsat = __popc(mask);
+  if (nsat > slots || (mask >> W) != 0u) return;  // reported by the push
+  const int lane = lane_id(), warp = warp_id();
+  const unsigned lt = (1u << lane) - 1u;
+  const int r1 = W * n;
+  const int words_r1 = n + n / 32, words_k = K + K / 32;
+  const int nchunks = (r1 + nsat * K) / 32;  // n, K multiples of 32
+  const int per = (nchunks + NW - 1) / NW;
+  const int c0 = min(nchunks, warp * per), c1 = min(nchunks, c0 + per);
+  zero_hist(sm.sel);
+  if (threadIdx.x == 0) sm.flag = 0;
+  __syncthreads();
+  uint32_t *lk = sm.key + warp * SUB;
+  uint32_t *lv = sm.val + warp * SUB;
+  int cnt = 0;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  for (int c = c0; c < c1; ++c) {
+    const int fb = c * 32;
+    uint32_t key = 0u, gid = 0u;
+    if (fb < r1) {
+      const int r = fb / n, j = fb - r * n + lane;
+      if (((mask >> r) & 1u) == 0u) {
+        const int32_t *row = packed + ((int64_t)r * T + t) * words_r1;
+        const uint32_t w = static_cast<uint32_t>(__ldg(row + j));
+        const uint32_t plane = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
+        key = bprime_key(w);
+        gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
+      }
+    } else {
+      const int q = fb - r1;
+      const int s = q / K, j = q - s * K + lane;
+      const int32_t *sl = recv + ((int64_t)t * slots + s) * words_k;
+      const uint32_t w = static_cast<uint32_t>(sl[j]);
+      const uint32_t plane = static_cast<uint32_t>(sl[K + ((j - lane) >> 5)]);
+      key = bprime_key(w);
+      gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)nth_set_bit(mask, s);
+    }
+    if ((key >> 16) < tau) key = 0u;  // below the round-1 cut (or empty)
+    const unsigned b = __ballot_sync(kFull, key != 0u);
+    if (cnt + __popc(b) > SUB) {  // warp-uniform
+      if (lane == 0) sm.flag = 1;
+      break;
+    }
+    if (key != 0u) {
+      const int pos = cnt + __popc(b & lt);
+      lk[pos] = key;
+      lv[pos] = gid;
+      kmn = min(kmn, key);
+      kmx = max(kmx, key);
+    }
+    cnt += __popc(b);
+  }
+  const WarpStats st{cnt, __reduce_min_sync(kFull, kmn), __reduce_max_sync(kFull, kmx)};
+  __syncthreads();
+  int32_t *out = ids + t * ld_out;
+  if (sm.flag == 0) {  // block-uniform
+    const bool dup = list_merge_emit<BLOCK, SUB>(
+        sm, Seg{warp * SUB, cnt}, K,
+        [&](int pos, int32_t v) {
+          if ((unsigned)pos < (unsigned)K) out[pos] = v;
+        },
+        st);
+    if (dup && status != nullptr && threadIdx.x == 0)
+      atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
+    return;
+  }
+  __syncthreads();
+  rescue_select_regs<BLOCK, KPT>(*reinterpret_cast<RescueSmem<BLOCK, KPT> *>(smem_raw), packed,
+                                 W, T, n, K, slots, mask, tau, recv, out, status);
+}
+
 template <int BLOCK, int KPT>
 int launch_rescue_select(const int32_t *packed, int W, int64_t T, int n, int K, int slots,
                          const int32_t *sat_word, const int32_t *recv, int32_t *ids,
                          int64_t ld_out, int32_t *status, cudaStream_t st) {
-  auto kern = rescue_select_kernel<BLOCK, KPT>;
-  const size_t smem = sizeof(RescueSmem<BLOCK, KPT>);
+  constexpr int SUB = 512;  // list of (BLOCK / 32) x 512 entries
+  auto kern = rescue_select_kernel<BLOCK, KPT, SUB>;
+  const size_t smem = sizeof(RescueSmem<BLOCK, KPT>) > sizeof(ListSmem<BLOCK, SUB>)
+                          ? sizeof(RescueSmem<BLOCK, KPT>)
+                          : sizeof(ListSmem<BLOCK, SUB>);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   kern<<<dim3(static_cast<unsigned>(T)), BLOCK, smem, st>>>(packed, W, T, n, K, slots, sat_word,
                                                             recv, ids, ld_out, status);

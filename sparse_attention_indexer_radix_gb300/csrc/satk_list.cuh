@@ -282,6 +282,54 @@ __device__ void list_topk_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, P
   for (int q = nsel + (int)threadIdx.x; q < K; q += BLOCK) fill(q);
 }
 
+// Merge select on a list whose values are global ids: the K best entries
+// under (key desc, id asc) -- a select on the key, then, when the K-th key
+// is tied, a select on ~id among the tied entries -- emitted in list order
+// as out(rank, id), then out(rank, -1) up to K.  When one (key, id) is
+// repeated across the cut, all its copies are left out (fewer than K ids)
+// and the call returns true.
+template <int BLOCK, int SUB, class Out>
+__device__ bool list_merge_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, Out out,
+                                WarpStats pre = stats_unknown()) {
+  const Sel s1 = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, K, sm.sel, 8, pre);
+  if (s1.take_all || !s1.tie) {  // block-uniform: no tie at the K-th key (the usual case)
+    const bool all_keys = s1.take_all;
+    const uint32_t T1 = s1.T;
+    const int n1 = list_emit1<BLOCK>(
+        [&](int i) {
+          const uint32_t k = sm.key[i];
+          return k != 0u && (all_keys || k >= T1);
+        },
+        sg,
+        [&](int rank, int i) {
+          if ((unsigned)rank < (unsigned)K) out(rank, static_cast<int32_t>(sm.val[i]));
+        },
+        sm.sel);
+    for (int q = max(0, n1) + (int)threadIdx.x; q < K; q += BLOCK) out(q, -1);
+    return false;
+  }
+  const Sel s2 = list_select<BLOCK>(
+      [&](int i) { return sm.key[i] == s1.T ? 0xffffffffu - sm.val[i] : 0u; }, sg, s1.need,
+      sm.sel);
+  const uint32_t T1 = s1.T, t2 = s2.T;
+  const bool tie2 = s2.tie;
+  const int2 tot = list_emit<BLOCK>(
+      [&](int i) -> int {
+        const uint32_t k = sm.key[i];
+        if (k == 0u) return 0;
+        if (k != T1) return k > T1 ? 1 : 0;
+        const uint32_t k2 = 0xffffffffu - sm.val[i];
+        return (tie2 ? k2 > t2 : k2 >= t2) ? 1 : 0;
+      },
+      sg,
+      [&](int rank, int i, int2) {
+        if ((unsigned)rank < (unsigned)K) out(rank, static_cast<int32_t>(sm.val[i]));
+      },
+      [](int, int, int2) {}, sm.sel);
+  for (int q = max(0, tot.x) + (int)threadIdx.x; q < K; q += BLOCK) out(q, -1);
+  return tie2;
+}
+
 // ------------------------------------------------------- thresholds ------
 
 // The float whose ordered key is the smallest key >= T among the keys a

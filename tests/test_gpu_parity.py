@@ -405,6 +405,25 @@ def test_decode_merge_long_rank_rows(k):
     _compare_decode(got, want, f"decode long rank rows k={k}")
 
 
+def test_decode_rescue_massive_ties():
+    """Four saturated ranks whose pushed lists tie with the round-1 cut:
+    every pushed word scores >= tau16, so the filtered rescue list overflows
+    and the row takes the register select over every slot; the other ranks
+    hold a single value.  Bit-exact against the oracle."""
+    W, T, S, n, k = 8, 4, 5000, 256, 2048
+    g = torch.Generator().manual_seed(31)
+    x = torch.full((W, T, S), 0.5)
+    for r in range(4):
+        for t in range(T):
+            pos = torch.randperm(S, generator=g)[:300]
+            x[r, t, pos] = 4.0 + torch.rand(300, generator=g)
+    lg = x.to(torch.bfloat16)
+    got = _decode_gpu(lg, n, k)
+    want = _decode_oracle(lg, n, k)
+    _compare_decode(got, want, "decode massive ties")
+    assert int(((want["sat"] >> 16) != 0).sum()) > 0, "the case must saturate"
+
+
 def test_decode_merge_row_ends_nan_and_small():
     W, T, S, n, k = 4, 12, 3000, 64, 512
     lg, _, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, skew_count=120, seed=77)
