@@ -64,10 +64,13 @@ def _load():
                                                 vp, vp, ctypes.c_int]
             lib.oracle_rescue.argtypes = [vp, i32, i64, i32, i32, vp, i64, i64,
                                           vp, vp, vp, vp, i64, vp, ctypes.c_int]
+            lib.oracle_topk_rows_sorted.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp,
+                                                    i32, vp, i64, ctypes.c_int]
             lib.oracle_emit_rows.argtypes = [vp, i64, i32, i64, i32, i32, vp, vp, i64,
                                              i64, i32, i32, i64, vp, i64, vp, vp]
             for f in ("oracle_topk_rows", "oracle_dcp_pack", "oracle_merge_pairs",
-                      "oracle_merge_packed", "oracle_rescue", "oracle_emit_rows"):
+                      "oracle_merge_packed", "oracle_rescue", "oracle_emit_rows",
+                      "oracle_topk_rows_sorted"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -94,10 +97,11 @@ def _check(rc, name):
         raise ValueError(f"{name}: oracle rejected its arguments (rc={rc})")
 
 
-def topk_rows(x, k, row_ends=None, out=None, ld_out=None, nthreads=0):
+def topk_rows(x, k, row_ends=None, out=None, ld_out=None, nthreads=0, sorted=False):
     """Exact per-row top-K of ``x`` ([rows, cols] float32, or uint16 holding
     bf16 bits).  Returns (or fills) an int32 [rows, ld_out] array; only
-    columns [0, k) of each row are written."""
+    columns [0, k) of each row are written.  ``sorted``: the same ids in
+    descending score order, ties by ascending column."""
     x = np.ascontiguousarray(x)
     if x.dtype == np.float32:
         dt = F32
@@ -111,8 +115,8 @@ def topk_rows(x, k, row_ends=None, out=None, ld_out=None, nthreads=0):
         out = np.full((rows, ld_out), -7, dtype=np.int32)
     assert out.dtype == np.int32 and out.flags.c_contiguous
     re = _c(row_ends, np.int32)
-    rc = _load().oracle_topk_rows(_ptr(x), dt, rows, cols, cols, _ptr(re), k,
-                                  _ptr(out), out.shape[1], nthreads)
+    f = _load().oracle_topk_rows_sorted if sorted else _load().oracle_topk_rows
+    rc = f(_ptr(x), dt, rows, cols, cols, _ptr(re), k, _ptr(out), out.shape[1], nthreads)
     _check(rc, "topk_rows")
     return out
 

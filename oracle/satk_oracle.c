@@ -154,7 +154,7 @@ static int i64_cmp(const void *pa, const void *pb) {
  */
 static int64_t row_topk_layout(const float *vals, const unsigned char *is_nan,
                                int64_t end, int32_t k, int64_t *cols_out,
-                               item_t *scratch) {
+                               item_t *scratch, int sorted) {
   int64_t n = 0;
   for (int64_t c = 0; c < end; ++c) {
     if (is_nan[c]) continue;
@@ -165,6 +165,11 @@ static int64_t row_topk_layout(const float *vals, const unsigned char *is_nan,
   }
   /* the plain definition: full sort, score desc, column asc */
   qsort(scratch, (size_t)n, sizeof(item_t), item_cmp);
+  if (sorted) { /* score-sorted layout: the first min(n, k) of the sort */
+    const int64_t m = n < k ? n : k;
+    for (int64_t i = 0; i < m; ++i) cols_out[i] = scratch[i].id;
+    return m;
+  }
   if (n < k) {
     for (int64_t i = 0; i < n; ++i) cols_out[i] = scratch[i].id;
     qsort(cols_out, (size_t)n, sizeof(int64_t), i64_cmp);
@@ -189,6 +194,7 @@ typedef struct {
   int32_t k;
   int32_t *out;
   int64_t ld_out;
+  int sorted;
 } topk_ctx_t;
 
 static void topk_row(void *p, int64_t row) {
@@ -211,7 +217,7 @@ static void topk_row(void *p, int64_t row) {
     vals[col] = v;
     nan_flag[col] = isnan(v) ? 1 : 0;
   }
-  int64_t n = row_topk_layout(vals, nan_flag, end, c->k, sel, scratch);
+  int64_t n = row_topk_layout(vals, nan_flag, end, c->k, sel, scratch, c->sorted);
   int32_t *o = c->out + row * c->ld_out;
   for (int64_t i = 0; i < n; ++i) o[i] = (int32_t)sel[i];
   for (int64_t i = n; i < c->k; ++i) o[i] = -1;
@@ -227,7 +233,21 @@ int oracle_topk_rows(const void *x, int dtype, int64_t rows, int64_t cols,
   if (!x || !out || rows < 0 || cols < 0 || ld < cols || k < 1 ||
       ld_out < k || (dtype != OR_F32 && dtype != OR_BF16))
     return -1;
-  topk_ctx_t c = {x, dtype, cols, ld, row_ends, k, out, ld_out};
+  topk_ctx_t c = {x, dtype, cols, ld, row_ends, k, out, ld_out, 0};
+  for_rows(rows, nthreads, topk_row, &c);
+  return 0;
+}
+
+/* The same chosen set in score order: descending score, ties by ascending
+ * column (the plain full sort's first min(n_valid, K) entries), then -1. */
+int oracle_topk_rows_sorted(const void *x, int dtype, int64_t rows,
+                            int64_t cols, int64_t ld, const int32_t *row_ends,
+                            int32_t k, int32_t *out, int64_t ld_out,
+                            int nthreads) {
+  if (!x || !out || rows < 0 || cols < 0 || ld < cols || k < 1 ||
+      ld_out < k || (dtype != OR_F32 && dtype != OR_BF16))
+    return -1;
+  topk_ctx_t c = {x, dtype, cols, ld, row_ends, k, out, ld_out, 1};
   for_rows(rows, nthreads, topk_row, &c);
   return 0;
 }
@@ -529,7 +549,7 @@ static void rescue_row(void *p, int64_t t) {
       vals[col] = bf16_value(lrow[col]);
       nf[col] = bf16_is_nan(lrow[col]) ? 1 : 0;
     }
-    int64_t cnt = row_topk_layout(vals, nf, end, c->k, sel, scratch);
+    int64_t cnt = row_topk_layout(vals, nf, end, c->k, sel, scratch, 0);
     int32_t *slot = c->recv + (t * slots + s) * rw;
     for (int64_t i = 0; i < rw; ++i) slot[i] = 0;
     for (int64_t i = 0; i < cnt; ++i) {

@@ -449,3 +449,38 @@ def test_emit_rows_max_blocks_and_bad_requests():
     assert rows[0].tolist() == [1000, 1001, 2000, 2001, -1] and valid[0] == 4 and status == 0
     rows, valid, status = oracle.emit_rows(ids, 4, 1, np.array([-1], np.int32), table, 2, 100)
     assert rows[0].tolist() == [-1] * 5 and valid[0] == 0 and status == 4
+
+
+# ------------------------------------------------------- sorted top-K --
+
+def test_topk_sorted_exhaustive_tiny_alphabet():
+    """Score-sorted output: brute force over every row of 4 values from
+    {NaN, -inf, -1, -0, +0, 1, +inf} (with repeats) against Python's sorted()
+    on (-ordered key, column), for every K and row end."""
+    alphabet = [float("nan"), float("-inf"), -1.0, -0.0, 0.0, 1.0, float("inf")]
+
+    def okey(v):  # -0.0 below +0.0
+        return (v, math.copysign(1.0, v))
+    for vals in itertools.product(alphabet, repeat=4):
+        x = np.array([vals], dtype=np.float32)
+        for end in range(5):
+            for k in (1, 2, 3, 4, 5):
+                got = oracle.topk_rows(x, k, row_ends=np.array([end], np.int32), sorted=True)[0]
+                valid = [c for c in range(end) if not math.isnan(vals[c])]
+                order = sorted(valid, key=lambda c: (tuple(-t for t in okey(vals[c])), c))
+                want = order[:k] + [-1] * (k - min(k, len(order)))
+                assert got.tolist() == want, (vals, end, k, got.tolist(), want)
+
+
+def test_topk_sorted_is_the_unsorted_set():
+    x, ends = inputs.prefill(rows=12, cols=3000, seed=5)
+    x, ends = x.numpy(), ends.numpy()
+    x[3, ::7] = x[3, 1]  # ties
+    for k in (1, 64, 512, 4000):
+        a = oracle.topk_rows(x, k, row_ends=ends)
+        b = oracle.topk_rows(x, k, row_ends=ends, sorted=True)
+        for i in range(12):
+            assert sorted(a[i].tolist()) == sorted(b[i].tolist())
+            ids = b[i][b[i] >= 0]
+            s = x[i, ids]
+            assert np.all(s[:-1] >= s[1:])  # non-increasing scores
