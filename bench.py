@@ -355,6 +355,18 @@ def _stage_robust(dev, flush, peak, satk):
         x, ends = inputs.prefill_shifted(8192, 8192, mode, device=dev)
         one(f"dist_{mode}_8192x8192_f32_K512", x, ends)
         del x
+    # the score-sorted output option on the prefill 8192-column width
+    x, ends = inputs.prefill(rows=ROWS, cols=8192, seed=1236, device=dev)
+    out = torch.empty((ROWS, K), dtype=torch.int32, device=dev)
+    fn = lambda: satk.topk_rows(x, K, row_ends=ends, out=out, sorted=True)  # noqa: E731
+    for _ in range(3):
+        fn()
+    ms = timed_calls(fn, 10, flush)
+    nb = int(ends.clamp(min=0).sum().item()) * 4 + ROWS * K * 4
+    st["sorted_4096x8192_f32_K512"] = {"us": ms * 1e3, "rows_per_s": ROWS / (ms * 1e-3),
+                                       "gbs": nb / (ms * 1e-3) / 1e9,
+                                       "frac": nb / (ms * 1e-3) / 1e9 / peak}
+    del x
     # decode-shaped few long rows (the DCP kernels page: the cluster variant
     # of its selector for <= 6 rows at >= 512K columns): bf16, K = 384
     x, ends = inputs.prefill(rows=4, cols=524288, seed=1260, device=dev, causal=False,

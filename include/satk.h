@@ -94,6 +94,19 @@ int satk_topk_rows(const void *logits, int dtype, int64_t rows, int64_t cols,
                    int32_t *out, int64_t ld_out, satk_stream_t stream);
 
 /*
+ * satk_topk_rows_sorted -- satk_topk_rows with the chosen ids in score
+ * order: descending score, ties by ascending column (a score-sorted output
+ * option; the pages' selectors never sort, [P2 DCPTopkSelectKernel: "a
+ * fixed order"]).  The chosen set, the -1 tail, the untouched columns
+ * [k, ld_out), the arguments and the errors are those of satk_topk_rows.
+ * Slower: every row takes one CTA and a shared-memory sort of the k ids.
+ */
+int satk_topk_rows_sorted(const void *logits, int dtype, int64_t rows,
+                          int64_t cols, int64_t ld_logits,
+                          const int32_t *row_ends, int32_t k, int32_t *out,
+                          int64_t ld_out, satk_stream_t stream);
+
+/*
  * satk_dcp_pack -- pack a local top-n into B' rows [P2 DCPTopkPackKernel,
  * dcp_topk_pack_indices].
  *
@@ -268,6 +281,10 @@ const char *satk_status_string(int rc);
 int topk_rows(const void *logits, int dtype, int64_t rows, int64_t cols,
               int64_t ld_logits, const int32_t *row_ends, int32_t k,
               int32_t *out, int64_t ld_out, satk_stream_t stream);
+int topk_rows_sorted(const void *logits, int dtype, int64_t rows,
+                     int64_t cols, int64_t ld_logits, const int32_t *row_ends,
+                     int32_t k, int32_t *out, int64_t ld_out,
+                     satk_stream_t stream);
 int dcp_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
              int64_t ld_logits, const int32_t *local_idx, int64_t ld_idx,
              int32_t n, const int32_t *row_ends, int32_t *packed,

@@ -27,8 +27,8 @@ MERGE_MAX_CANDIDATES = 32768
 
 EXPORTS = ("satk_topk_rows", "satk_dcp_pack", "satk_dcp_merge_select",
            "satk_dcp_rescue_select", "satk_rescue_recv_words", "satk_status_string",
-           "satk_dcp_emit_rows", "topk_rows", "dcp_pack", "dcp_merge_select",
-           "dcp_rescue_select", "dcp_emit_rows")
+           "satk_dcp_emit_rows", "satk_topk_rows_sorted", "topk_rows", "topk_rows_sorted",
+           "dcp_pack", "dcp_merge_select", "dcp_rescue_select", "dcp_emit_rows")
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +51,7 @@ def lib() -> ctypes.CDLL:
             vp, i32, i64, c_int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
             sigs = {
                 "satk_topk_rows": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
+                "satk_topk_rows_sorted": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
                 "satk_dcp_pack": [vp, i64, i64, i64, vp, i64, i32, vp, vp, vp],
                 "satk_dcp_merge_select": [vp, c_int, i32, i64, i32, i32, vp, i64, vp, vp, vp],
                 "satk_dcp_rescue_select": [vp, i32, i64, i32, i32, vp, i64, i64, vp, vp, vp, vp,
@@ -97,11 +98,13 @@ def _rowmajor_2d(t, name):
 
 
 def topk_rows(logits: torch.Tensor, k: int, row_ends: torch.Tensor | None = None,
-              out: torch.Tensor | None = None) -> torch.Tensor:
+              out: torch.Tensor | None = None, *, sorted: bool = False) -> torch.Tensor:
     """Exact top-k column ids of each row of ``logits`` ([rows, cols] float32
     or bfloat16, any row stride).  ``out`` (int32 [rows, >= k], any row
     stride) receives the ids in columns [0, k); columns past k are never
-    written.  Returns ``out`` (allocated [rows, k] when not given)."""
+    written.  ``sorted`` orders them by descending score, ties by ascending
+    column (satk_topk_rows_sorted).  Returns ``out`` (allocated [rows, k]
+    when not given)."""
     _need_cuda(logits, row_ends, out)
     _rowmajor_2d(logits, "logits")
     if logits.dtype == torch.float32:
@@ -121,9 +124,10 @@ def topk_rows(logits: torch.Tensor, k: int, row_ends: torch.Tensor | None = None
         raise SatkError("row_ends must be contiguous int32 [rows]")
     ld = logits.stride(0) if rows > 1 else max(cols, 1)
     ld_out = out.stride(0) if rows > 1 else out.shape[1]
-    rc = lib().satk_topk_rows(_ptr(logits), dt, rows, cols, ld, _ptr(row_ends), k, _ptr(out),
-                              ld_out, _stream(logits.device))
-    _check(rc, "satk_topk_rows")
+    f = lib().satk_topk_rows_sorted if sorted else lib().satk_topk_rows
+    rc = f(_ptr(logits), dt, rows, cols, ld, _ptr(row_ends), k, _ptr(out), ld_out,
+           _stream(logits.device))
+    _check(rc, "satk_topk_rows_sorted" if sorted else "satk_topk_rows")
     return out
 
 

@@ -50,6 +50,13 @@ extern "C" int topk_rows(const void *logits, int dtype, int64_t rows, int64_t co
   return satk_topk_rows(logits, dtype, rows, cols, ld_logits, row_ends, k, out, ld_out, stream);
 }
 
+extern "C" int topk_rows_sorted(const void *logits, int dtype, int64_t rows, int64_t cols,
+                                int64_t ld_logits, const int32_t *row_ends, int32_t k,
+                                int32_t *out, int64_t ld_out, satk_stream_t stream) {
+  return satk_topk_rows_sorted(logits, dtype, rows, cols, ld_logits, row_ends, k, out, ld_out,
+                               stream);
+}
+
 extern "C" int dcp_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S, int64_t ld_logits,
                         const int32_t *local_idx, int64_t ld_idx, int32_t n,
                         const int32_t *row_ends, int32_t *packed, satk_stream_t stream) {

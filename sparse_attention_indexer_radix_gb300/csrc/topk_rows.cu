@@ -63,6 +63,12 @@ int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_en
   return launch_status();
 }
 
+// Byte offset of the sorted kernel's composite buffer after the list.
+template <int SUB>
+__host__ __device__ constexpr size_t sorted_buf_offset() {
+  return (sizeof(ListSmem<kBlock, SUB>) + 15) / 16 * 16;
+}
+
 // Short rows: one warp per row (satk_warp.cuh), kWarpRowsPerCta rows per
 // CTA, seven CTAs per SM (their workspaces fill the shared memory).
 template <typename T, int ALIGN>
@@ -199,6 +205,85 @@ int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *r
                                                  st);
 }
 
+// ------------------------------------------------------- score-sorted --
+
+// In-place bitonic sort of P (a power of two) 64-bit values in shared
+// memory into descending order.  Every thread of the block takes part.
+template <int BLOCK, int P>
+__device__ void bitonic_sort_desc(uint64_t *buf) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += BLOCK) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const uint64_t a = buf[lo], b = buf[hi];
+        // blocks whose size bit is clear end descending, the others
+        // ascending; at size == P every block ends descending
+        const bool desc = (lo & size) == 0;
+        if (desc ? a < b : a > b) {
+          buf[lo] = b;
+          buf[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// The chosen set of topk_rows_kernel in score order: the row path emits
+// (key << 32 | ~column) composites into shared memory, a bitonic sort puts
+// them in descending order (key desc, then column asc), and the columns are
+// written out; positions without a candidate hold 0 and become -1.
+template <typename T, int SUB, int ALIGN, int P>
+__global__ void __launch_bounds__(kBlock, 4) topk_rows_sorted_kernel(
+    const T *__restrict__ x, int64_t ld, int cols, const int32_t *__restrict__ row_ends, int K,
+    int32_t *__restrict__ out, int64_t ld_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &sm = *reinterpret_cast<ListSmem<kBlock, SUB> *>(smem_raw);
+  uint64_t *buf = reinterpret_cast<uint64_t *>(smem_raw + sorted_buf_offset<SUB>());
+  const int64_t row = blockIdx.x;
+  zero_hist(sm.sel);
+  for (int i = threadIdx.x; i < P; i += kBlock) buf[i] = 0u;
+  __syncthreads();
+  topk_row<T, kBlock, SUB, ALIGN>(
+      x + row * ld, row_end_of(row_ends, row, cols), K,
+      [&](int pos, int i) {
+        if ((unsigned)pos < (unsigned)K)
+          buf[pos] = (static_cast<uint64_t>(sm.key[i]) << 32) | (0xffffffffu - sm.val[i]);
+      },
+      [](int) {}, sm);
+  __syncthreads();
+  bitonic_sort_desc<kBlock, P>(buf);
+  int32_t *o = out + row * ld_out;
+  for (int q = threadIdx.x; q < K; q += kBlock) {
+    const uint64_t c = buf[q];
+    o[q] = c == 0u ? -1 : static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(c));
+  }
+}
+
+template <typename T, int SUB, int ALIGN, int P>
+int launch_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
+                  int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_sorted_kernel<T, SUB, ALIGN, P>;
+  const size_t smem = sorted_buf_offset<SUB>() + sizeof(uint64_t) * P;
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(rows)), kBlock, smem, st>>>(x, ld, cols, row_ends, K, out,
+                                                                ld_out);
+  return launch_status();
+}
+
+template <typename T, int ALIGN>
+int launch_rows_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
+                       int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  if (K <= 512)
+    return launch_sorted<T, 512, ALIGN, 512>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (K <= 1024)
+    return launch_sorted<T, 512, ALIGN, 1024>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (K <= 2048)
+    return launch_sorted<T, 1024, ALIGN, 2048>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  return launch_sorted<T, 1024, ALIGN, 4096>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+}
+
 // Widest load every row start allows: 32 or 16 bytes, else element loads.
 inline int row_alignment(const void *x, int64_t ld_bytes) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(x);
@@ -209,6 +294,34 @@ inline int row_alignment(const void *x, int64_t ld_bytes) {
 
 }  // namespace
 }  // namespace satk
+
+extern "C" int satk_topk_rows_sorted(const void *logits, int dtype, int64_t rows, int64_t cols,
+                                     int64_t ld_logits, const int32_t *row_ends, int32_t k,
+                                     int32_t *out, int64_t ld_out, satk_stream_t stream) {
+  using namespace satk;
+  if (logits == nullptr || out == nullptr || rows < 0 || cols < 0 || ld_logits < cols ||
+      k < 1 || k > SATK_TOPK_MAX_K || ld_out < k || cols > INT_MAX || rows > INT_MAX ||
+      (dtype != SATK_F32 && dtype != SATK_BF16))
+    return SATK_EINVAL;
+  if (rows == 0) return SATK_OK;
+  const cudaStream_t st = as_stream(stream);
+  const int c = static_cast<int>(cols);
+  if (dtype == SATK_F32) {
+    const float *x = static_cast<const float *>(logits);
+    switch (row_alignment(x, ld_logits * 4)) {
+      case 32:
+        return launch_rows_sorted<float, 32>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+      case 16:
+        return launch_rows_sorted<float, 16>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+      default:
+        return launch_rows_sorted<float, 0>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+    }
+  }
+  const uint16_t *x = static_cast<const uint16_t *>(logits);
+  if (row_alignment(x, ld_logits * 2) != 0)
+    return launch_rows_sorted<uint16_t, 16>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+  return launch_rows_sorted<uint16_t, 0>(x, rows, c, ld_logits, row_ends, k, out, ld_out, st);
+}
 
 extern "C" int satk_topk_rows(const void *logits, int dtype, int64_t rows, int64_t cols,
                               int64_t ld_logits, const int32_t *row_ends, int32_t k,

@@ -63,8 +63,9 @@ NULL = None
 
 
 @no_gpu
-def test_topk_rows_rejects(lib):
-    f = lib.satk_topk_rows
+@pytest.mark.parametrize("name", ["satk_topk_rows", "satk_topk_rows_sorted"])
+def test_topk_rows_rejects(lib, name):
+    f = getattr(lib, name)
     ok = dict(x=P, dt=0, rows=4, cols=100, ld=100, re=NULL, k=8, out=P, ldo=8)
 
     def call(**kw):

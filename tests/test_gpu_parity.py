@@ -39,7 +39,8 @@ def host_view(x: torch.Tensor) -> np.ndarray:
     return bits_of(x) if x.dtype == torch.bfloat16 else x.cpu().numpy()
 
 
-def run_topk(x: torch.Tensor, k: int, ends: torch.Tensor | None, ld_out: int, ld_x=None):
+def run_topk(x: torch.Tensor, k: int, ends: torch.Tensor | None, ld_out: int, ld_x=None,
+             sorted=False):
     """GPU and oracle outputs for x ([rows, cols], CPU tensor)."""
     rows, cols = x.shape
     if ld_x is not None and ld_x != cols:
@@ -49,9 +50,10 @@ def run_topk(x: torch.Tensor, k: int, ends: torch.Tensor | None, ld_out: int, ld
     else:
         xg = x.to(DEV)
     out = torch.full((rows, ld_out), CANARY, dtype=torch.int32, device=DEV)
-    satk.topk_rows(xg, k, row_ends=None if ends is None else ends.to(DEV), out=out)
+    satk.topk_rows(xg, k, row_ends=None if ends is None else ends.to(DEV), out=out, sorted=sorted)
     want = np.full((rows, ld_out), CANARY, dtype=np.int32)
-    oracle.topk_rows(host_view(x), k, row_ends=None if ends is None else ends.numpy(), out=want)
+    oracle.topk_rows(host_view(x), k, row_ends=None if ends is None else ends.numpy(), out=want,
+                     sorted=sorted)
     return out.cpu().numpy(), want
 
 
@@ -188,6 +190,26 @@ def test_topk_decode_shaped_few_rows():
     for k in (384, 2048):
         got, want = run_topk(x, k, ends, k)
         assert_rows_equal(got, want, f"few rows k={k}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("cols,ld", [(3000, 3000), (20001, 20003), (70000, 70000)])
+def test_topk_sorted(dtype, cols, ld):
+    """Score-sorted output: every K class (sort widths 512 to 4096), short
+    rows, ties, NaN and signed zeros, aligned and unaligned rows."""
+    rows = 12
+    x, _ = inputs.prefill(rows=rows, cols=cols, seed=cols + 3, dtype=torch.float32)
+    g = torch.Generator().manual_seed(cols)
+    ends = torch.randint(0, cols + 1, (rows,), generator=g, dtype=torch.int32)
+    ends[:4] = torch.tensor([0, 5, 600, cols], dtype=torch.int32)
+    x[4] = torch.randint(0, 3, (cols,), generator=g).float()  # three levels
+    x[5, ::2] = float("nan")
+    x[6, :] = -0.0
+    x[6, 1::3] = 0.0
+    x = x.to(dtype)
+    for k in (1, 300, 512, 1000, 2048, 4096):
+        got, want = run_topk(x, k, ends, k + 2, ld_x=ld, sorted=True)
+        assert_rows_equal(got, want, f"sorted {dtype} cols={cols} k={k}")
 
 
 @pytest.mark.parametrize("mode", ["plus100", "times1e-8"])
