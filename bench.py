@@ -172,12 +172,23 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """The largest of the ranks' values (the job's time is its slowest
+    rank's); on the process group's own device (CUDA for NCCL, CPU for
+    gloo)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_rows_per_s(rows_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput of `world` replicas, each processing
+    rows_per_step rows per step: every rank's rows over the slowest rank's
+    time (weak scaling)."""
+    return rows_per_step * steps * world / (max_ms * 1e-3)
 
 
 # ------------------------------------------------------------- CPU oracle --
@@ -464,7 +475,7 @@ def run_gpu(args):
     per_width_ms = [statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1])
                                     for s in range(args.steps)) for j in range(len(widths))]
     rows_step = rows * len(widths)
-    value = rows_step * args.steps * world / (total_ms * 1e-3)
+    value = replica_rows_per_s(rows_step, args.steps, world, total_ms)
 
     # ---- end to end: pinned host inputs -> device -> ids -> host, every step
     host_in = [(x.cpu().pin_memory(), e.cpu().pin_memory()) for (_, x, e, _) in data]
@@ -491,7 +502,7 @@ def run_gpu(args):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b), world)
-    e2e_value = rows_step * e_steps * world / (e2e_ms * 1e-3)
+    e2e_value = replica_rows_per_s(rows_step, e_steps, world, e2e_ms)
 
     # ---- roofline of the dominant kernel (largest share of the step)
     j = int(np.argmax(per_width_ms))
