@@ -76,7 +76,7 @@ __device__ __forceinline__ PassOut cluster_find_threshold(cg::cluster_group &cl,
     cnt[q] = 0u;
     if (g < NG) {
       const int bin = NB - 1 - (g * 32 + lane);
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < C; ++c) cnt[q] += cluster_word(cl, sm.hist + bin, c);
     }
     gs[q] = static_cast<int>(__reduce_add_sync(kFull, cnt[q]));
@@ -188,7 +188,10 @@ __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &
   int need = K;
   uint32_t prefix = 0u;
   int pbits = 0;
-  const int digit = total > kListLong ? kListDigitLong : kListDigitShort;
+  // 8-bit digits: 256 bins, one per thread of the first 256, so each thread
+  // reads C remote words per pass, all in flight at once (11-bit digits
+  // made it 8 x C dependent remote reads per thread per pass)
+  const int digit = kListDigitShort;
   while (pbits < b) {  // cluster-uniform: b, digit, need and the digits agree
     const int width = (b - pbits) < digit ? (b - pbits) : digit;
     const int shift = b - pbits - width;
@@ -203,9 +206,7 @@ __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &
       }
     }
     cl.sync();  // every CTA's histogram complete
-    const PassOut p = digit == kListDigitLong
-                          ? cluster_find_threshold<BLOCK, (1 << kListDigitLong), C>(cl, sm, need)
-                          : cluster_find_threshold<BLOCK, (1 << kListDigitShort), C>(cl, sm, need);
+    const PassOut p = cluster_find_threshold<BLOCK, (1 << kListDigitShort), C>(cl, sm, need);
     cl.sync();  // every CTA done reading the histograms
     for (int i = threadIdx.x; i <= static_cast<int>(dmask); i += BLOCK) sm.hist[i] = 0u;
     __syncthreads();
