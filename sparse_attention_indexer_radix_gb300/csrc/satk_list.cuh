@@ -330,6 +330,118 @@ __device__ bool list_merge_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, 
   return tie2;
 }
 
+// ------------------------------------------------------ one warp alone --
+//
+// The select above at warp scale: no block barrier, only the calling warp
+// (all 32 lanes) and a 256-bin histogram of its own.
+
+// The digit d of a 256-bin histogram (descending) with
+// above(d) < need <= above(d) + hist[d]; d = -1 when fewer than need keys
+// were counted.  Zeroes every bin.  Lane l reads bins 255 - (32 j + l), so
+// each of its eight reads is conflict-free.
+struct WarpDigit {
+  int d, above, cnt;
+};
+__device__ __forceinline__ WarpDigit warp_find_digit(uint32_t *hist, int need) {
+  const int lane = lane_id();
+  uint32_t c[8];
+  int gs[8];
+  int total = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int bin = 255 - (32 * j + lane);
+    c[j] = hist[bin];
+    hist[bin] = 0u;
+    gs[j] = static_cast<int>(__reduce_add_sync(kFull, c[j]));
+    total += gs[j];
+  }
+  WarpDigit r{-1, 0, 0};
+  if (total < need) return r;
+  int cum = 0, jc = 0;
+  uint32_t cj = 0u;
+  bool found = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // warp-uniform
+    if (!found && cum + gs[j] >= need) {
+      found = true;
+      jc = j;
+      cj = c[j];
+    } else if (!found) {
+      cum += gs[j];
+    }
+  }
+  const int incl = warp_incl_scan(static_cast<int>(cj));
+  const int before = cum + incl - static_cast<int>(cj);
+  const unsigned hit = __ballot_sync(kFull, before < need && before + static_cast<int>(cj) >= need);
+  const int src = __ffs(hit) - 1;
+  r.d = 255 - (32 * jc + src);
+  r.above = __shfl_sync(kFull, before, src);
+  r.cnt = __shfl_sync(kFull, static_cast<int>(cj), src);
+  return r;
+}
+
+// Outcome of a warp select (as Sel in satk_device.cuh).
+struct WarpSel {
+  uint32_t T;
+  int need;
+  bool tie, take_all;
+};
+
+// The K largest of the n keys key[0, n) (all non-zero), mn / mx their
+// smallest and largest: radix select with 8-bit digits cut from key - mn
+// over the bit-length of mx - mn.  With max_passes the passes may stop
+// early; T is then the start of the threshold digit (at least K keys >= T).
+__device__ __forceinline__ WarpSel warp_list_select(const uint32_t *key, int n, int K,
+                                                    uint32_t mn, uint32_t mx, uint32_t *hist,
+                                                    int max_passes) {
+  const int lane = lane_id();
+  WarpSel s{1u, 0, false, false};
+  if (n < K) {
+    s.take_all = true;
+    return s;
+  }
+  const uint32_t span = mx - mn;
+  const int b = span == 0u ? 0 : 32 - __clz(span);
+  int need = K;
+  uint32_t prefix = 0u;
+  int pbits = 0;
+  while (pbits < b) {
+    const int width = (b - pbits) < 8 ? (b - pbits) : 8;
+    const int shift = b - pbits - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int i = lane; i < n; i += 32) {
+      const uint32_t rel = key[i] - mn;
+      if (pbits == 0 || (rel >> (shift + width)) == prefix)
+        atomicAdd(hist + ((rel >> shift) & dmask), 1u);
+    }
+    __syncwarp();
+    const WarpDigit p = warp_find_digit(hist, need);
+    __syncwarp();
+    need -= p.above;
+    prefix = (prefix << width) | static_cast<uint32_t>(p.d);
+    pbits += width;
+    if (p.cnt == need || --max_passes == 0) {
+      s.T = mn + (prefix << shift);
+      s.need = need;
+      return s;
+    }
+  }
+  s.T = mn + prefix;  // every bit resolved: the K-th key, `need` of its ties wanted
+  s.need = need;
+  s.tie = true;
+  return s;
+}
+
+// Warp-wide smallest and largest of the lanes' non-zero keys, and their count.
+struct WarpRange {
+  int n;
+  uint32_t mn, mx;
+};
+__device__ __forceinline__ WarpRange warp_range(int n, uint32_t mn, uint32_t mx) {
+  return WarpRange{static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(n))),
+                   __reduce_min_sync(kFull, mn), __reduce_max_sync(kFull, mx)};
+}
+
 // ------------------------------------------------------- thresholds ------
 
 // The float whose ordered key is the smallest key >= T among the keys a
