@@ -3,15 +3,18 @@
 // ([Perf][DSA] Use DeepSelect for eligible sparse-indexer prefill chunks,
 // vLLM PR #57206: Purpose, Test Plan).
 //
-// One CTA of 256 threads per row; the row path of satk_rows.cuh reads each
-// valid column from HBM once (sampled threshold, filtered collection into
-// a shared-memory list, exact select on the list).
+// Every path reads each valid column from HBM once: a sampled threshold, a
+// filtered collection into a shared-memory list, an exact select on the
+// list.  The launch picks the path by shape:
+//  - rows of a few thousand columns: one warp per row (satk_warp.cuh);
+//  - few long rows: a cluster of 2-8 CTAs per row (satk_cluster.cuh);
+//  - otherwise one CTA of 128 or 256 threads per row (satk_rows.cuh).
+// satk_topk_rows_sorted runs the CTA path and sorts the chosen ids by score.
 #include <climits>
-
 #include <cmath>
 
-#include "satk_host.hpp"
 #include "satk_cluster.cuh"
+#include "satk_host.hpp"
 #include "satk_rows.cuh"
 #include "satk_warp.cuh"
 
