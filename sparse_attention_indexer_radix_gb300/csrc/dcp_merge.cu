@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   // ---- select: by score, then by global id among ties with the K-th
   int32_t *out = ids + t * ld_out;
   const bool dup = list_merge_emit<BLOCK, SUB>(
-      sm, sg, K, [&](int pos, int32_t v) { out[pos] = v; }, ok ? st : stats_unknown());
+      sm, sg, K, [&](int pos, int32_t v) { out[pos] = v; }, ok ? st : stats_unknown()).dup;
   if (dup && status != nullptr && threadIdx.x == 0) atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
 }
 
@@ -398,6 +398,101 @@ int launch_pairs(const int32_t *cand, int W, int64_t T, int n, int K, int32_t *i
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   kern<<<dim3(static_cast<unsigned>(T)), BLOCK, smem, st>>>(reinterpret_cast<const int2 *>(cand),
                                                             W, T, n, K, ids, ld_out, status);
+  return launch_status();
+}
+
+// ---------------------------------------------------- packed, list engine --
+//
+// The packed round-1 merge when every candidate fits the list (W * n <=
+// 16 * kPackedSub): each warp copies its stretch of the flat range (32
+// candidates per step, in flat order) into its list segment, skipping
+// empty words -- no threshold is needed -- and the list merge select picks
+// K.  tau16 is the ord16 of the smallest chosen key (0 below K chosen);
+// rank r is saturated iff all its n words are listed with ord16 > tau16,
+// counted per rank from the list.
+constexpr int kPackedBlock = 512;
+constexpr int kPackedSub = 512;
+
+__global__ void __launch_bounds__(kPackedBlock) packed_merge_list_kernel(
+    const int32_t *__restrict__ cand, int W, int64_t T, int n, int K,
+    int32_t *__restrict__ ids, int64_t ld_out, int32_t *__restrict__ sat_word,
+    int32_t *__restrict__ status) {
+  constexpr int BLOCK = kPackedBlock, SUB = kPackedSub, NW = BLOCK / 32;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &sm = *reinterpret_cast<ListSmem<BLOCK, SUB> *>(smem_raw);
+  __shared__ int above[16];  // per rank: words listed with ord16 > tau16
+  const int64_t t = blockIdx.x;
+  const int lane = lane_id(), warp = warp_id();
+  const unsigned lt = (1u << lane) - 1u;
+  const int words = n + n / 32;
+  const int nchunks = W * n / 32;  // n % 32 == 0
+  const int per = (nchunks + NW - 1) / NW;
+  const int c0 = min(nchunks, warp * per), c1 = min(nchunks, c0 + per);
+  zero_hist(sm.sel);
+  if (threadIdx.x < 16) above[threadIdx.x] = 0;
+  __syncthreads();
+  uint32_t *lk = sm.key + warp * SUB;
+  uint32_t *lv = sm.val + warp * SUB;
+  int cnt = 0;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  for (int c = c0; c < c1; ++c) {  // per * 32 <= SUB: no overflow
+    const int fb = c * 32;
+    const int r = fb / n, j = fb - r * n + lane;
+    const int32_t *row = cand + ((int64_t)r * T + t) * words;
+    const uint32_t w = static_cast<uint32_t>(__ldg(row + j));
+    const uint32_t plane = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
+    const uint32_t key = bprime_key(w);
+    const unsigned b = __ballot_sync(kFull, key != 0u);
+    if (key != 0u) {
+      const int pos = cnt + __popc(b & lt);
+      lk[pos] = key;
+      lv[pos] = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
+      kmn = min(kmn, key);
+      kmx = max(kmx, key);
+    }
+    cnt += __popc(b);
+  }
+  const WarpStats st{cnt, __reduce_min_sync(kFull, kmn), __reduce_max_sync(kFull, kmx)};
+  __syncthreads();
+  int32_t *out = ids + t * ld_out;
+  const Seg sg{warp * SUB, cnt};
+  const ListMergeOut m = list_merge_emit<BLOCK, SUB, true>(
+      sm, sg, K,
+      [&](int pos, int32_t v) {
+        if ((unsigned)pos < (unsigned)K) out[pos] = v;
+      },
+      st);
+  int bits = m.dup ? SATK_STATUS_DUPLICATE_KEYS : 0;
+  if (sat_word != nullptr) {
+    const uint32_t tau = (m.nsel == K) ? (m.kmin >> 16) : 0u;
+    for (int j = 0; j < sg.rounds(); ++j) {
+      const int i = j * 32 + lane;
+      if (i < sg.cnt && (sm.key[sg.base + i] >> 16) > tau)
+        atomicAdd(&above[sm.val[sg.base + i] % static_cast<uint32_t>(W)], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t mask = 0u;
+      for (int q = 0; q < W; ++q)
+        if (above[q] == n) mask |= 1u << q;
+      const int slots = (K - 1) / n;
+      if (__popc(mask) > slots) {
+        mask = 0u;  // more saturated ranks than slots: keep round 1
+        bits |= SATK_STATUS_SLOTS_EXCEEDED;
+      }
+      sat_word[t] = static_cast<int32_t>((mask << 16) | tau);
+    }
+  }
+  if (bits != 0 && status != nullptr && threadIdx.x == 0) atomicOr(status, bits);
+}
+
+int launch_packed_list(const int32_t *cand, int W, int64_t T, int n, int K, int32_t *ids,
+                       int64_t ld_out, int32_t *sat_word, int32_t *status, cudaStream_t st) {
+  auto kern = packed_merge_list_kernel;
+  const size_t smem = sizeof(ListSmem<kPackedBlock, kPackedSub>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(T)), kPackedBlock, smem, st>>>(cand, W, T, n, K, ids, ld_out,
+                                                                   sat_word, status);
   return launch_status();
 }
 
@@ -416,6 +511,8 @@ template <bool PACKED>
 int dispatch_merge(const int32_t *cand, int W, int64_t T, int n, int K, int32_t *ids,
                    int64_t ld_out, int32_t *sat_word, int32_t *status, cudaStream_t st) {
   const int total = W * n;
+  if (PACKED && total <= (kPackedBlock / 32) * kPackedSub)
+    return launch_packed_list(cand, W, T, n, K, ids, ld_out, sat_word, status, st);
   if (total <= 512 * 2)
     return launch_merge<512, 2, PACKED>(cand, W, T, n, K, ids, ld_out, sat_word, status, st);
   if (total <= 512 * 8)

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
         [&](int pos, int32_t v) {
           if ((unsigned)pos < (unsigned)K) out[pos] = v;
         },
-        st);
+        st).dup;
     if (dup && status != nullptr && threadIdx.x == 0)
       atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
     return;

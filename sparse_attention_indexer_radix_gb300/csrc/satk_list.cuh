@@ -288,13 +288,29 @@ __device__ void list_topk_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, P
 // as out(rank, id), then out(rank, -1) up to K.  When one (key, id) is
 // repeated across the cut, all its copies are left out (fewer than K ids)
 // and the call returns true.
-template <int BLOCK, int SUB, class Out>
-__device__ bool list_merge_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, Out out,
-                                WarpStats pre = stats_unknown()) {
+struct ListMergeOut {
+  bool dup;       // a repeated (key, id) sat on the cut
+  int nsel;       // ids emitted before the -1 fill
+  uint32_t kmin;  // smallest chosen key (with WANT_MIN; 0xffffffff when none)
+};
+
+template <int BLOCK, int SUB, bool WANT_MIN = false, class Out>
+__device__ ListMergeOut list_merge_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, Out out,
+                                        WarpStats pre = stats_unknown()) {
   const Sel s1 = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, K, sm.sel, 8, pre);
   if (s1.take_all || !s1.tie) {  // block-uniform: no tie at the K-th key (the usual case)
     const bool all_keys = s1.take_all;
     const uint32_t T1 = s1.T;
+    uint32_t kmin = 0xffffffffu;
+    if (WANT_MIN) {
+      uint32_t m = 0xffffffffu;
+      for (int j = 0; j < sg.rounds(); ++j) {
+        const int i = j * 32 + lane_id();
+        const uint32_t k = i < sg.cnt ? sm.key[sg.base + i] : 0u;
+        if (k != 0u && (all_keys || k >= T1)) m = min(m, k);
+      }
+      kmin = block_min<BLOCK>(m, sm.sel);
+    }
     const int n1 = list_emit1<BLOCK>(
         [&](int i) {
           const uint32_t k = sm.key[i];
@@ -306,7 +322,7 @@ __device__ bool list_merge_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, 
         },
         sm.sel);
     for (int q = max(0, n1) + (int)threadIdx.x; q < K; q += BLOCK) out(q, -1);
-    return false;
+    return ListMergeOut{false, min(n1, K), kmin};
   }
   const Sel s2 = list_select<BLOCK>(
       [&](int i) { return sm.key[i] == s1.T ? 0xffffffffu - sm.val[i] : 0u; }, sg, s1.need,
@@ -327,7 +343,9 @@ __device__ bool list_merge_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, 
       },
       [](int, int, int2) {}, sm.sel);
   for (int q = max(0, tot.x) + (int)threadIdx.x; q < K; q += BLOCK) out(q, -1);
-  return tie2;
+  // with a tie the K-th key itself is chosen, unless its copies were all
+  // left out as repeats (then fewer than K ids)
+  return ListMergeOut{tie2, min(tot.x, K), WANT_MIN ? T1 : 0xffffffffu};
 }
 
 // ------------------------------------------------------ one warp alone --
