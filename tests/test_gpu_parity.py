@@ -461,6 +461,24 @@ def test_decode_merge_row_ends_nan_and_small():
     _compare_decode(got, want, "decode small")
 
 
+def test_packed_merge_wide():
+    """W * n above the list engine's capacity: the register merge (16 ranks
+    of 1024 candidates), ids, saturation words and status against the
+    oracle."""
+    W, T, S, n, k = 16, 4, 5000, 1024, 2048
+    lg, _, _ = inputs.decode_merge(W=W, rows=T, S=S, n=n, k=k, skew_count=1500, seed=41)
+    bits = bits_of(lg)
+    local = oracle.topk_rows(bits.reshape(W * T, S), n)
+    packed = oracle.dcp_pack(bits.reshape(W * T, S), local).reshape(W, T, n + n // 32)
+    sat = torch.zeros(T, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ids = satk.dcp_merge_select(torch.from_numpy(packed).to(DEV), k, packed=True, sat_word=sat,
+                                status=st)
+    w_ids, w_sat, w_st = oracle.merge_packed(packed, k)
+    assert_rows_equal(ids.cpu().numpy(), w_ids, "wide packed merge")
+    assert np.array_equal(sat.cpu().numpy(), w_sat) and int(st.item()) == w_st
+
+
 def test_packed_merge_out_of_contract_words():
     """Repeated words (a NaN row's arbitrary ids on the page) and more
     saturated ranks than slots: bit-exact status, ids and sat_word.  Row 0
