@@ -9,17 +9,21 @@
 // one device buffer, so the push is an ordinary kernel writing `recv` and
 // stream order replaces the flags: nothing waits on anything.
 //
-// rescue_push_kernel  : one CTA per (row, slot); slot s of a row with a
+// rescue_push_kernel  : one CTA per (row, slot) (a cluster of CTAs for long
+//                       rank rows); slot s of a row with a
 //                       non-zero mask takes the s-th set bit's rank, runs the
 //                       row top-K on that rank's bf16 logits (the streaming
 //                       path of satk_rows.cuh) and writes the list in the B'
 //                       layout to recv[t, s].
 // rescue_select_kernel: one CTA per row; a zero mask costs one load.  The
 //                       candidates are the round-1 words of the ranks outside
-//                       the mask scoring at or above tau16, then the pushed
-//                       lists; the merge select of satk_merge.cuh picks K.
+//                       the mask, then the pushed lists, those scoring at or
+//                       above tau16 filtered into the shared-memory list; the
+//                       list merge select picks K (the register select of
+//                       satk_merge.cuh when the list would overflow).
 #include <climits>
 
+#include "satk_cluster.cuh"
 #include "satk_host.hpp"
 #include "satk_merge.cuh"
 #include "satk_rows.cuh"
@@ -28,6 +32,12 @@ namespace satk {
 namespace {
 
 constexpr int kPushBlock = 256;
+// Rank rows of at least kPushClusterCols columns are pushed by clusters of
+// kPushCluster CTAs (measured on the decode workload: rescue 56 -> 49 us
+// with four, 54 us with eight); the grid holds every (row, slot) pair.
+constexpr int kPushCluster = 4;
+constexpr int64_t kPushClusterCols = 32768;
+constexpr int64_t kPushClusterMaxPairs = (int64_t{1} << 31) / (2 * kPushCluster);
 
 __device__ __forceinline__ int nth_set_bit(uint32_t mask, int s) {
   for (int q = 0; q < s; ++q) mask &= mask - 1u;
@@ -87,6 +97,65 @@ int launch_push(const uint16_t *logits, int64_t S, int64_t ld, int W, int64_t T,
   const size_t smem = sizeof(ListSmem<kPushBlock, SUB>) + sizeof(uint32_t) * (size_t)(K + K / 32);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   kern<<<dim3(static_cast<unsigned>(T * slots)), kPushBlock, smem, st>>>(
+      logits, S, ld, W, T, K, slots, row_ends, sat_word, recv, status);
+  return launch_status();
+}
+
+// The push on a cluster of C CTAs per (row, slot) for long rank rows (only
+// a few (row, rank) pairs push, so one CTA each leaves most SMs idle): the
+// row path of satk_cluster.cuh, each CTA writing its own words of the B'
+// list straight to recv, plane bits by atomics on words CTA 0 zeroes before
+// the first cluster barrier.  A (row, slot) without a push leaves as a
+// whole cluster (the decision reads only the row's sat_word).
+template <int SUB, int ALIGN, int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kPushBlock, 1024 / kPushBlock)
+    rescue_push_cluster_kernel(const uint16_t *__restrict__ logits, int64_t S, int64_t ld, int W,
+                               int64_t T, int K, int slots,
+                               const int32_t *__restrict__ row_ends,
+                               const int32_t *__restrict__ sat_word, int32_t *__restrict__ recv,
+                               int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &cs = *reinterpret_cast<ClusterSmem<kPushBlock, SUB> *>(smem_raw);
+  cg::cluster_group cl = cg::this_cluster();
+  const int64_t q = blockIdx.x / C;
+  const int64_t t = q / slots;
+  const int s = static_cast<int>(q % slots);
+  const uint32_t mask = static_cast<uint32_t>(sat_word[t]) >> 16;
+  if (mask == 0u) return;
+  const int nsat = __popc(mask);
+  if (nsat > slots || (mask >> W) != 0u) {
+    if (s == 0 && cl.block_rank() == 0 && threadIdx.x == 0 && status != nullptr)
+      atomicOr(status, SATK_STATUS_SLOTS_EXCEEDED);
+    return;
+  }
+  if (s >= nsat) return;
+  const int r = nth_set_bit(mask, s);
+  int64_t end = S < SATK_LOCAL_INDEX_LIMIT ? S : SATK_LOCAL_INDEX_LIMIT;
+  if (row_ends != nullptr && (int64_t)row_ends[(int64_t)r * T + t] < end)
+    end = row_ends[(int64_t)r * T + t];
+  if (end < 0) end = 0;
+  uint32_t *dst = reinterpret_cast<uint32_t *>(recv) + ((int64_t)t * slots + s) * (K + K / 32);
+  if (cl.block_rank() == 0)
+    for (int i = threadIdx.x; i < K / 32; i += kPushBlock) dst[K + i] = 0u;
+  zero_hist(cs.ls.sel);
+  __syncthreads();
+  cluster_topk_row<uint16_t, kPushBlock, SUB, ALIGN, C>(
+      cl, logits + ((int64_t)r * T + t) * ld, static_cast<int>(end), K,
+      [&](int pos, uint32_t key, int col) {
+        dst[pos] = key | (0xffffu - (static_cast<uint32_t>(col) & 0xffffu));
+        if ((col >> 16) & 1) atomicOr(dst + K + pos / 32, 1u << (pos & 31));
+      },
+      [&](int pos) { dst[pos] = 0u; }, cs);
+}
+
+template <int SUB, int ALIGN, int C>
+int launch_push_cluster(const uint16_t *logits, int64_t S, int64_t ld, int W, int64_t T, int K,
+                        int slots, const int32_t *row_ends, const int32_t *sat_word,
+                        int32_t *recv, int32_t *status, cudaStream_t st) {
+  auto kern = rescue_push_cluster_kernel<SUB, ALIGN, C>;
+  const size_t smem = sizeof(ClusterSmem<kPushBlock, SUB>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(T * slots * C)), kPushBlock, smem, st>>>(
       logits, S, ld, W, T, K, slots, row_ends, sat_word, recv, status);
   return launch_status();
 }
@@ -287,7 +356,14 @@ extern "C" int satk_dcp_rescue_select(const int32_t *packed, int32_t W, int64_t 
   // 1. pushes of the saturated ranks
   const bool vec = aligned16(logits_bf16) && (ld_logits * 2) % 16 == 0;
   int rc;
-  if (k <= 1024)
+  if (S >= kPushClusterCols && vec && T * slots <= kPushClusterMaxPairs) {
+    if (k <= 1024)
+      rc = launch_push_cluster<512, 16, kPushCluster>(logits_bf16, S, ld_logits, W, T, k, slots,
+                                                      row_ends, sat_word, recv, status, st);
+    else
+      rc = launch_push_cluster<1024, 16, kPushCluster>(logits_bf16, S, ld_logits, W, T, k, slots,
+                                                       row_ends, sat_word, recv, status, st);
+  } else if (k <= 1024)
     rc = vec ? launch_push<512, 16>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
                                       sat_word, recv, status, st)
              : launch_push<512, 0>(logits_bf16, S, ld_logits, W, T, k, slots, row_ends,
