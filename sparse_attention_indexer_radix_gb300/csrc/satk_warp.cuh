@@ -5,7 +5,8 @@
 // Here every warp owns one row and a small shared-memory workspace, and
 // never waits on another warp, so an SM holds 28 rows at once.  The steps
 // are those of the CTA path (satk_rows.cuh) at warp scale:
-//  1. threshold from a sample of kWarpSample columns (6 runs of 256);
+//  1. threshold from a sample of up to kWarpSample columns (runs of 256,
+//     as few as keep the expected list within bounds for the row's length);
 //  2. one filtered pass that records keys and columns of the columns at or
 //     above it in the warp's list, in column order, with the copy engine
 //     one batch ahead of the loads (bulk L2 prefetch);
@@ -37,43 +38,60 @@ struct WarpRowSmem {
 static_assert(kWarpSample <= kWarpList + kWarpList / 2, "the sample must fit the list area");
 
 // Sample threshold of a row of end > kWarpList columns: the r-th largest key
-// of kWarpSample sampled columns -- kWarpSample / 256 runs of 32 8-column
-// groups, one vector load per lane and run, spread evenly over the row --
+// of the sampled columns -- runs of 32 8-column groups, one vector load per
+// lane and run, spread evenly over the row, as many runs (at most
+// kWarpSample / 256) as keep the expected list plus four standard
+// deviations within kWarpList for this row's length --
 // r = mu + 4 sqrt(mu) + 4 with mu = K * samples / end (as the CTA path);
 // 1 when the sample holds fewer than r valid keys.  Two digit passes.
 template <typename T, int ALIGN>
 __device__ __forceinline__ uint32_t warp_sample_threshold(const T *__restrict__ xr, int end,
                                                           int K, WarpRowSmem &ws) {
-  constexpr int NRUNS = kWarpSample / 256;
+  constexpr int MAXRUNS = kWarpSample / 256;
   const int lane = lane_id();
   const int ngroups = end / 8;  // >= 128: end > kWarpList
+  // fewest runs of 256 columns whose expected list (K r / mu) plus four
+  // standard deviations fits the list; shorter rows need fewer samples
+  int nruns = MAXRUNS;
+  for (int q = 1; q < MAXRUNS; ++q) {  // warp-uniform
+    const float mu = static_cast<float>(K) * (256 * q) / static_cast<float>(end);
+    const float r = ceilf(mu + 4.f * sqrtf(mu) + 4.f);
+    const float list = static_cast<float>(K) * r / mu;
+    if (list + 4.f * list * rsqrtf(r) <= static_cast<float>(kWarpList)) {
+      nruns = q;
+      break;
+    }
+  }
+  const int S = 256 * nruns;
   uint32_t *sk = ws.buf;
   uint32_t mn = 0xffffffffu, mx = 0u;
 #pragma unroll
-  for (int q = 0; q < NRUNS; ++q) {
-    // 32-bit: q * ngroups < NRUNS * 2**13 for the rows this path takes
-    const int g0 = min((q * ngroups) / NRUNS, ngroups - 32);
-    Group8<T, ALIGN> grp;
-    grp.load(xr + static_cast<size_t>(g0 + lane) * 8);
+  for (int q = 0; q < MAXRUNS; ++q) {
+    if (q < nruns) {
+      // 32-bit: q * ngroups < MAXRUNS * 2**13 for the rows this path takes
+      const int g0 = min((q * ngroups) / nruns, ngroups - 32);
+      Group8<T, ALIGN> grp;
+      grp.load(xr + static_cast<size_t>(g0 + lane) * 8);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t k = key_of_raw<T>(grp.raw(e));
-      sk[(q * 8 + e) * 32 + lane] = k;
-      mn = min(mn, k);
-      mx = max(mx, k);
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t k = key_of_raw<T>(grp.raw(e));
+        sk[(q * 8 + e) * 32 + lane] = k;
+        mn = min(mn, k);
+        mx = max(mx, k);
+      }
     }
   }
   mn = __reduce_min_sync(kFull, mn);
   mx = __reduce_max_sync(kFull, mx);
   __syncwarp();
-  const float mu = static_cast<float>(K) * kWarpSample / static_cast<float>(end);
+  const float mu = static_cast<float>(K) * S / static_cast<float>(end);
   int r = static_cast<int>(ceilf(mu + 4.f * sqrtf(mu) + 4.f));
-  r = r < 1 ? 1 : (r > kWarpSample ? kWarpSample : r);
-  int m = kWarpSample;
+  r = r < 1 ? 1 : (r > S ? S : r);
+  int m = S;
   if (mn == 0u) {  // NaN samples (key 0): compact the valid keys to the front
     m = 0;
     mn = 0xffffffffu;
-    for (int i0 = 0; i0 < kWarpSample; i0 += 32) {
+    for (int i0 = 0; i0 < S; i0 += 32) {
       const uint32_t k = sk[i0 + lane];
       const unsigned b = __ballot_sync(kFull, k != 0u);
       __syncwarp();
