@@ -159,11 +159,14 @@ struct SelectSmem {
   int wtot[4][BLOCK / 32];  // scan scratch: [0] thresholds, [1]-[3] by caller
   int scal[8];              // broadcast scalars
   uint32_t red[BLOCK / 32]; // reductions
+  uint32_t fin[64];         // the few keys of a threshold digit (list select)
+  int fcnt;                 // their count, kept zero between uses
 };
 
 template <int BLOCK>
 __device__ __forceinline__ void zero_hist(SelectSmem<BLOCK> &sm) {
   for (int i = threadIdx.x; i < 2048; i += BLOCK) sm.hist[i] = 0u;
+  if (threadIdx.x == 0) sm.fcnt = 0;
 }
 
 // Histogram add of digit d for lanes with m set.  With AGG, lanes holding

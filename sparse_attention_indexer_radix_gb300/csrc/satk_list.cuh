@@ -58,6 +58,8 @@ __device__ __forceinline__ WarpStats stats_unknown() { return WarpStats{-1, 0u, 
 constexpr int kListDigitShort = 8;
 constexpr int kListDigitLong = 11;
 constexpr int kListLong = 1024;
+// At most this many keys in the threshold digit are ranked directly.
+constexpr int kListFinish = 64;
 
 // Radix select of the K largest keys among the list entries gk(i) != 0 of
 // this thread's segment.  Outcome as Sel (see satk_device.cuh); the
@@ -145,7 +147,61 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
     need -= p.above;
     prefix = (prefix << width) | static_cast<uint32_t>(p.d);
     pbits += width;
-    if (p.cnt == need || --max_passes == 0) {
+    if (p.cnt == need) {
+      r.T = mn + (prefix << shift);
+      r.need = need;
+      return r;
+    }
+    if (p.cnt <= kListFinish && pbits < b) {  // block-uniform
+      // a few keys left in the threshold digit: rank them on one warp
+      // instead of more digit passes over the whole list
+      for (int j = 0; j < sg.rounds(); ++j) {
+        const int i = j * 32 + lane;
+        const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
+        if (k != 0u && ((k - mn) >> shift) == prefix) {
+          const int pos = atomicAdd(&sm.fcnt, 1);
+          if (pos < kListFinish) sm.fin[pos] = k;
+        }
+      }
+      __syncthreads();
+      if (warp_id() == 0) {
+        const int c = p.cnt;
+        // lane l ranks fin[l] and fin[l + 32]: the need-th largest v has
+        // gt(v) < need <= gt(v) + eq(v)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = lane + 32 * h;
+          if (q < c) {
+            const uint32_t x = sm.fin[q];
+            int gt = 0, eq = 0;
+            for (int i = 0; i < c; ++i) {
+              const uint32_t f = sm.fin[i];
+              gt += f > x ? 1 : 0;
+              eq += f == x ? 1 : 0;
+            }
+            if (gt < need && need <= gt + eq) {  // every copy of v writes the same
+              sm.scal[4] = static_cast<int>(x);
+              sm.scal[5] = gt;
+              sm.scal[6] = eq;
+            }
+          }
+        }
+        if (lane == 0) sm.fcnt = 0;
+      }
+      __syncthreads();
+      const uint32_t v = static_cast<uint32_t>(sm.scal[4]);
+      const int gt = sm.scal[5], eq = sm.scal[6];
+      if (gt + eq == need) {  // exactly K keys >= v
+        r.T = v;
+        r.need = need;
+      } else {  // v is the K-th key, need - gt of its ties wanted
+        r.T = v;
+        r.need = need - gt;
+        r.tie = true;
+      }
+      return r;
+    }
+    if (--max_passes == 0) {
       r.T = mn + (prefix << shift);
       r.need = need;
       return r;
