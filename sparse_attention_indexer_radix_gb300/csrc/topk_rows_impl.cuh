@@ -1,0 +1,313 @@
+// topk_rows_impl.cuh -- the kernels and launch code of satk_topk_rows and
+// satk_topk_rows_sorted, templated on the element type and the row
+// alignment.  Each (type, alignment) pair is instantiated in a translation
+// unit of its own (topk_rows_f32_a32.cu, ...), which keeps the build parallel;
+// topk_rows.cu holds the C entry points.
+//
+// Every path reads each valid column from HBM once: a sampled threshold, a
+// filtered collection into a shared-memory list, an exact select on the
+// list.  The launch picks the path by shape:
+//  - rows of a few thousand columns: one warp per row (satk_warp.cuh);
+//  - few long rows: a cluster of 2-8 CTAs per row (satk_cluster.cuh);
+//  - otherwise one CTA of 128 or 256 threads per row (satk_rows.cuh).
+// The score-sorted variant runs the CTA path and sorts the chosen ids.
+#pragma once
+
+#include <climits>
+#include <cmath>
+
+#include "satk_cluster.cuh"
+#include "satk_host.hpp"
+#include "satk_rows.cuh"
+#include "satk_warp.cuh"
+
+namespace satk {
+namespace {
+
+// 256 threads per row; rows of at most 16384 columns with K <= 512 take
+// 128 (more rows resident per SM, shorter barriers: short rows are bound by
+// the per-row select, not by the stream).
+constexpr int kBlock = 256;
+constexpr int kShortBlock = 128;
+constexpr int kShortCols = 16384;
+
+__device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, int cols) {
+  if (row_ends == nullptr) return cols;
+  const int e = row_ends[row];
+  return e < 0 ? 0 : (e > cols ? cols : e);
+}
+
+template <typename T, int BLOCK, int SUB, int ALIGN>
+__global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) topk_rows_kernel(const T *__restrict__ x, int64_t ld,
+                                                          int cols,
+                                                          const int32_t *__restrict__ row_ends,
+                                                          int K, int32_t *__restrict__ out,
+                                                          int64_t ld_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &sm = *reinterpret_cast<ListSmem<BLOCK, SUB> *>(smem_raw);
+  const int64_t row = blockIdx.x;
+  const int end = row_end_of(row_ends, row, cols);
+  zero_hist(sm.sel);
+  __syncthreads();
+  int32_t *o = out + row * ld_out;
+  topk_row<T, BLOCK, SUB, ALIGN>(
+      x + row * ld, end, K,
+      [&](int pos, int i) {
+        if ((unsigned)pos < (unsigned)K) o[pos] = static_cast<int32_t>(sm.val[i]);
+      },
+      [&](int pos) { o[pos] = -1; }, sm);
+}
+
+template <typename T, int BLOCK, int SUB, int ALIGN>
+int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
+           int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_kernel<T, BLOCK, SUB, ALIGN>;
+  const size_t smem = sizeof(ListSmem<BLOCK, SUB>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(rows)), BLOCK, smem, st>>>(x, ld, cols, row_ends, K, out,
+                                                               ld_out);
+  return launch_status();
+}
+
+// Byte offset of the sorted kernel's composite buffer after the list.
+template <int SUB>
+__host__ __device__ constexpr size_t sorted_buf_offset() {
+  return (sizeof(ListSmem<kBlock, SUB>) + 15) / 16 * 16;
+}
+
+// Short rows: one warp per row (satk_warp.cuh), kWarpRowsPerCta rows per
+// CTA, seven CTAs per SM (their workspaces fill the shared memory).
+template <typename T, int ALIGN>
+__global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
+    topk_rows_warp_kernel(const T *__restrict__ x, int64_t rows, int64_t ld, int cols,
+                          const int32_t *__restrict__ row_ends, int K,
+                          int32_t *__restrict__ out, int64_t ld_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int warp = warp_id();
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpRowsPerCta + warp;
+  if (row >= rows) return;  // warp-uniform; the warps never synchronise
+  WarpRowSmem &ws = reinterpret_cast<WarpRowSmem *>(smem_raw)[warp];
+  for (int i = lane_id(); i < 256; i += 32) ws.hist[i] = 0u;
+  __syncwarp();
+  warp_topk_row<T, ALIGN>(x + row * ld, row_end_of(row_ends, row, cols), K, out + row * ld_out,
+                          ws);
+}
+
+template <typename T, int ALIGN>
+int launch_warp(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
+                int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_warp_kernel<T, ALIGN>;
+  const size_t smem = sizeof(WarpRowSmem) * kWarpRowsPerCta;
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  const int64_t grid = (rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta;
+  kern<<<dim3(static_cast<unsigned>(grid)), 32 * kWarpRowsPerCta, smem, st>>>(
+      x, rows, ld, cols, row_ends, K, out, ld_out);
+  return launch_status();
+}
+
+// Whether a row of `cols` columns keeps its sampled candidate list within
+// one warp's kWarpList entries: the expected list K r / mu (r and mu as in
+// the sample step) plus four standard deviations (about list / sqrt(r)) of
+// the r-th sample order statistic.  Rows that still overflow take the exact
+// path, so this only decides speed.
+inline bool warp_rows_fit(int cols, int K) {
+  if (K > 512 || cols > 65536) return false;
+  if (cols <= kWarpList) return true;
+  const double mu = static_cast<double>(K) * kWarpSample / cols;
+  const double r = std::ceil(mu + 4.0 * std::sqrt(mu) + 4.0);
+  const double list = K * r / mu;
+  return list + 4.0 * list / std::sqrt(r) <= kWarpList;
+}
+
+// Few long rows: a cluster of C CTAs per row (satk_cluster.cuh); the grid
+// is rows x C, CTA blockIdx.x % C of the cluster taking slice
+// blockIdx.x % C of row blockIdx.x / C.
+template <typename T, int BLOCK, int SUB, int ALIGN, int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(BLOCK, 1024 / BLOCK)
+    topk_rows_cluster_kernel(const T *__restrict__ x, int64_t ld, int cols,
+                             const int32_t *__restrict__ row_ends, int K,
+                             int32_t *__restrict__ out, int64_t ld_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &cs = *reinterpret_cast<ClusterSmem<BLOCK, SUB> *>(smem_raw);
+  cg::cluster_group cl = cg::this_cluster();
+  const int64_t row = blockIdx.x / C;
+  zero_hist(cs.ls.sel);
+  __syncthreads();
+  int32_t *o = out + row * ld_out;
+  cluster_topk_row<T, BLOCK, SUB, ALIGN, C>(
+      cl, x + row * ld, row_end_of(row_ends, row, cols), K,
+      [&](int pos, uint32_t, int col) { o[pos] = col; }, [&](int pos) { o[pos] = -1; }, cs);
+}
+
+template <typename T, int BLOCK, int SUB, int ALIGN, int C>
+int launch_cluster(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
+                   int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_cluster_kernel<T, BLOCK, SUB, ALIGN, C>;
+  const size_t smem = sizeof(ClusterSmem<BLOCK, SUB>);
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(rows * C)), BLOCK, smem, st>>>(x, ld, cols, row_ends, K,
+                                                                   out, ld_out);
+  return launch_status();
+}
+
+// Cluster size for `rows` rows when one CTA per row would fill fewer than
+// three waves of resident CTAs (0: no cluster): the smallest of 2, 4, 8
+// that reaches three waves, else 8.  A cluster adds barriers to every step
+// of a row, which only pays when the slices stay long: with at least one
+// full wave of rows, a slice under kClusterMinSlice bytes keeps one CTA per
+// row (measured: 1024 bf16 rows of 128 KB ran 2x slower on two-CTA
+// clusters, 1310 fp32 rows of 400 KB 1.35x faster, 256 bf16 rows of up to
+// 256 KB 3.2x faster on eight).
+constexpr int64_t kClusterMinSlice = 128 * 1024;
+
+template <typename T, int BLOCK, int SUB, int ALIGN>
+int cluster_size(int64_t rows, int cols) {
+  if (rows > INT32_MAX / 8 || cols < 8 * 2 * ListSmem<BLOCK, SUB>::CAP) return 0;
+  const int64_t resident =
+      resident_ctas(reinterpret_cast<const void *>(topk_rows_kernel<T, BLOCK, SUB, ALIGN>),
+                    BLOCK, sizeof(ListSmem<BLOCK, SUB>));
+  if (resident <= 0 || rows >= 3 * resident) return 0;
+  int c = 8;
+  for (int t = 2; t < 8; t *= 2)
+    if (rows * t >= 3 * resident) {
+      c = t;
+      break;
+    }
+  const int64_t slice = static_cast<int64_t>(cols) * static_cast<int64_t>(sizeof(T)) / c;
+  if (rows >= resident && slice < kClusterMinSlice) return 0;
+  return c;
+}
+
+template <typename T, int BLOCK, int SUB, int ALIGN>
+int launch_rows_cta(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
+                    int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  switch (cluster_size<T, BLOCK, SUB, ALIGN>(rows, cols)) {
+    case 2:
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 2>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                     st);
+    case 4:
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 4>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                     st);
+    case 8:
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 8>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                     st);
+    default:
+      return launch<T, BLOCK, SUB, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  }
+}
+
+// The list holds (BLOCK/32) warps x SUB candidates.
+template <typename T, int ALIGN>
+int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
+                int32_t *out, int64_t ld_out, cudaStream_t st) {
+  if (warp_rows_fit(cols, K))
+    return launch_warp<T, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (cols <= kShortCols && K <= 512)
+    return launch<T, kShortBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (K <= 1024)
+    return launch_rows_cta<T, kBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                  st);
+  return launch_rows_cta<T, kBlock, 1024, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                 st);
+}
+
+// ------------------------------------------------------- score-sorted --
+
+// In-place bitonic sort of P (a power of two) 64-bit values in shared
+// memory into descending order.  Every thread of the block takes part.
+template <int BLOCK, int P>
+__device__ void bitonic_sort_desc(uint64_t *buf) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += BLOCK) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const uint64_t a = buf[lo], b = buf[hi];
+        // blocks whose size bit is clear end descending, the others
+        // ascending; at size == P every block ends descending
+        const bool desc = (lo & size) == 0;
+        if (desc ? a < b : a > b) {
+          buf[lo] = b;
+          buf[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// The chosen set of topk_rows_kernel in score order: the row path emits
+// (key << 32 | ~column) composites into shared memory, a bitonic sort puts
+// them in descending order (key desc, then column asc), and the columns are
+// written out; positions without a candidate hold 0 and become -1.
+template <typename T, int SUB, int ALIGN, int P>
+__global__ void __launch_bounds__(kBlock, 4) topk_rows_sorted_kernel(
+    const T *__restrict__ x, int64_t ld, int cols, const int32_t *__restrict__ row_ends, int K,
+    int32_t *__restrict__ out, int64_t ld_out) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &sm = *reinterpret_cast<ListSmem<kBlock, SUB> *>(smem_raw);
+  uint64_t *buf = reinterpret_cast<uint64_t *>(smem_raw + sorted_buf_offset<SUB>());
+  const int64_t row = blockIdx.x;
+  zero_hist(sm.sel);
+  for (int i = threadIdx.x; i < P; i += kBlock) buf[i] = 0u;
+  __syncthreads();
+  topk_row<T, kBlock, SUB, ALIGN>(
+      x + row * ld, row_end_of(row_ends, row, cols), K,
+      [&](int pos, int i) {
+        if ((unsigned)pos < (unsigned)K)
+          buf[pos] = (static_cast<uint64_t>(sm.key[i]) << 32) | (0xffffffffu - sm.val[i]);
+      },
+      [](int) {}, sm);
+  __syncthreads();
+  bitonic_sort_desc<kBlock, P>(buf);
+  int32_t *o = out + row * ld_out;
+  for (int q = threadIdx.x; q < K; q += kBlock) {
+    const uint64_t c = buf[q];
+    o[q] = c == 0u ? -1 : static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(c));
+  }
+}
+
+template <typename T, int SUB, int ALIGN, int P>
+int launch_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
+                  int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_sorted_kernel<T, SUB, ALIGN, P>;
+  const size_t smem = sorted_buf_offset<SUB>() + sizeof(uint64_t) * P;
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  kern<<<dim3(static_cast<unsigned>(rows)), kBlock, smem, st>>>(x, ld, cols, row_ends, K, out,
+                                                                ld_out);
+  return launch_status();
+}
+
+template <typename T, int ALIGN>
+int launch_rows_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
+                       int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  if (K <= 512)
+    return launch_sorted<T, 512, ALIGN, 512>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (K <= 1024)
+    return launch_sorted<T, 512, ALIGN, 1024>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  if (K <= 2048)
+    return launch_sorted<T, 1024, ALIGN, 2048>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  return launch_sorted<T, 1024, ALIGN, 4096>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+}
+
+}  // namespace
+
+// One (type, alignment) pair of the row kernels: the entry points of
+// topk_rows.cu call these, defined in the per-pair translation units.
+int topk_rows_launch_f32_a32(const float *x, int64_t rows, int cols, int64_t ld,
+                             const int32_t *row_ends, int K, int32_t *out, int64_t ld_out,
+                             bool sorted, cudaStream_t st);
+int topk_rows_launch_f32_a16(const float *x, int64_t rows, int cols, int64_t ld,
+                             const int32_t *row_ends, int K, int32_t *out, int64_t ld_out,
+                             bool sorted, cudaStream_t st);
+int topk_rows_launch_f32_a0(const float *x, int64_t rows, int cols, int64_t ld,
+                            const int32_t *row_ends, int K, int32_t *out, int64_t ld_out,
+                            bool sorted, cudaStream_t st);
+int topk_rows_launch_bf16_a16(const uint16_t *x, int64_t rows, int cols, int64_t ld,
+                              const int32_t *row_ends, int K, int32_t *out, int64_t ld_out,
+                              bool sorted, cudaStream_t st);
+int topk_rows_launch_bf16_a0(const uint16_t *x, int64_t rows, int cols, int64_t ld,
+                             const int32_t *row_ends, int K, int32_t *out, int64_t ld_out,
+                             bool sorted, cudaStream_t st);
+
+}  // namespace satk
