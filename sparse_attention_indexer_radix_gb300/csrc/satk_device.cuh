@@ -282,6 +282,7 @@ struct Sel {
   int total;  // non-zero keys (valid when take_all)
   bool tie;
   bool take_all;
+  bool exact = false;  // !tie: T is itself a key, the smallest chosen one
 };
 
 // Radix select over register keys: 11-bit digits from the top; KEYBITS 32

@@ -191,9 +191,10 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
       __syncthreads();
       const uint32_t v = static_cast<uint32_t>(sm.scal[4]);
       const int gt = sm.scal[5], eq = sm.scal[6];
-      if (gt + eq == need) {  // exactly K keys >= v
+      if (gt + eq == need) {  // exactly K keys >= v, v the smallest of them
         r.T = v;
         r.need = need;
+        r.exact = true;
       } else {  // v is the K-th key, need - gt of its ties wanted
         r.T = v;
         r.need = need - gt;
@@ -310,7 +311,7 @@ __device__ void list_topk_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, P
   uint32_t v;
   if (sel.take_all) {
     v = 0u;
-  } else if (sel.tie) {
+  } else if (sel.tie || sel.exact) {
     v = sel.T;
   } else {
     uint32_t m = 0xffffffffu;
@@ -358,7 +359,9 @@ __device__ ListMergeOut list_merge_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg,
     const bool all_keys = s1.take_all;
     const uint32_t T1 = s1.T;
     uint32_t kmin = 0xffffffffu;
-    if (WANT_MIN) {
+    if (WANT_MIN && !all_keys && s1.exact) {
+      kmin = T1;  // the select found the smallest chosen key itself
+    } else if (WANT_MIN) {
       uint32_t m = 0xffffffffu;
       for (int j = 0; j < sg.rounds(); ++j) {
         const int i = j * 32 + lane_id();
