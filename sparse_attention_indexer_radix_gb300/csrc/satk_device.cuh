@@ -411,46 +411,4 @@ __device__ __forceinline__ int flat_pos(int i) {
   return warp_id() * (32 * KPT) + (i / VEC) * (32 * VEC) + lane_id() * VEC + (i % VEC);
 }
 
-// ------------------------------------------------------ row top-K emit ----
-
-// Given keys already in registers (0 = none) and the select outcome, emits
-// the row layout of the prefill top-K: slots strictly above the K-th key in
-// flat order, then slots equal to it in flat order up to K; put(pos, i)
-// stores slot i at output position pos, fill(pos) pads positions [n, K).
-template <int BLOCK, int KPT, int VEC, class GetKey, class Put, class Fill>
-__device__ void emit_topk_layout(GetKey gk, Put put, Fill fill, int K, const Sel &sel,
-                                 SelectSmem<BLOCK> &sm) {
-  uint32_t v;
-  if (sel.take_all) {
-    v = 0u;
-  } else if (sel.tie) {
-    v = sel.T;
-  } else {
-    uint32_t m = 0xffffffffu;
-#pragma unroll
-    for (int i = 0; i < KPT; ++i) {
-      const uint32_t k = gk(i);
-      if (k >= sel.T) m = min(m, k);
-    }
-    v = block_min<BLOCK>(m, sm);
-  }
-  const bool all = sel.take_all;
-  // group A: above v (every valid slot when taking all), group B: equal to v
-  auto cls = [&](int i) -> int {
-    const uint32_t k = gk(i);
-    if (k == 0u) return 0;
-    if (all) return 1;
-    return k > v ? 1 : (k == v ? 2 : 0);
-  };
-  // group B members fill the room left after group A, up to K
-  const int2 tot = ordered_emit<BLOCK, KPT, VEC>(
-      cls, [&](int rank, int i, int2) { put(rank, i); },
-      [&](int rank, int i, int2 t) {
-        if (rank < K - t.x) put(t.x + rank, i);
-      },
-      sm);
-  const int nsel = all ? max(0, min(tot.x, K)) : K;
-  for (int q = nsel + (int)threadIdx.x; q < K; q += BLOCK) fill(q);
-}
-
 }  // namespace satk

@@ -509,15 +509,6 @@ __device__ __forceinline__ WarpSel warp_list_select(const uint32_t *key, int n, 
   return s;
 }
 
-// Warp-wide smallest and largest of the lanes' non-zero keys, and their count.
-struct WarpRange {
-  int n;
-  uint32_t mn, mx;
-};
-__device__ __forceinline__ WarpRange warp_range(int n, uint32_t mn, uint32_t mx) {
-  return WarpRange{static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(n))),
-                   __reduce_min_sync(kFull, mn), __reduce_max_sync(kFull, mx)};
-}
 
 // ------------------------------------------------------- thresholds ------
 

@@ -65,16 +65,6 @@ __device__ __forceinline__ uint32_t load_raw(const T *p) {
   else
     return __ldg(reinterpret_cast<const unsigned short *>(p));
 }
-// element s of a 16-byte vector, as raw bits
-template <typename T>
-__device__ __forceinline__ uint32_t vec_raw(const uint4 &v, int s) {
-  constexpr int PER = KeyOf<T>::kVec / 4;  // elements per 32-bit word
-  const uint32_t w = s < PER ? v.x : s < 2 * PER ? v.y : s < 3 * PER ? v.z : v.w;
-  if constexpr (std::is_same<T, float>::value)
-    return w;
-  else
-    return (s & 1) ? (w >> 16) : (w & 0xffffu);
-}
 
 // ------------------------------------------------------------ threshold --
 

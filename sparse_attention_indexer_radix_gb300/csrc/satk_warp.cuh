@@ -37,6 +37,12 @@ struct WarpRowSmem {
 };
 static_assert(kWarpSample <= kWarpList + kWarpList / 2, "the sample must fit the list area");
 
+// Count, smallest and largest key of a warp's list (warp-uniform).
+struct WarpRange {
+  int n;
+  uint32_t mn, mx;
+};
+
 // Sample threshold of a row of end > kWarpList columns: the r-th largest key
 // of the sampled columns -- runs of 32 8-column groups, one vector load per
 // lane and run, spread evenly over the row, as many runs (at most
