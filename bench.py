@@ -483,43 +483,22 @@ def run_gpu(args):
     h2d = sum(x.numel() * x.element_size() + e.numel() * 4 for x, e in host_in)
     d2h = sum(o.numel() * 4 for o in host_out)
 
-    # The host link, not the kernels, bounds this loop: the inputs of width
-    # j+1 go up on their own stream while width j is selected, and the ids
-    # come down on a third stream.  Events keep every buffer's reuse behind
-    # its previous reader.
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in data]
-    ev_sel = [torch.cuda.Event() for _ in data]
-    ev_down = [torch.cuda.Event() for _ in data]
-
     def e2e_step():
         for j, (cols, x, ends, out) in enumerate(data):
             hx, he = host_in[j]
-            s_in.wait_event(ev_sel[j])  # the last select of x is done
-            with torch.cuda.stream(s_in):
-                x.copy_(hx, non_blocking=True)
-                ends.copy_(he, non_blocking=True)
-            ev_in[j].record(s_in)
-            stream.wait_event(ev_in[j])
-            stream.wait_event(ev_down[j])  # the last read-back of out is done
+            x.copy_(hx, non_blocking=True)
+            ends.copy_(he, non_blocking=True)
             satk.topk_rows(x, K, row_ends=ends, out=out)
-            ev_sel[j].record(stream)
-            s_out.wait_event(ev_sel[j])
-            with torch.cuda.stream(s_out):
-                host_out[j].copy_(out, non_blocking=True)
-            ev_down[j].record(s_out)
+            host_out[j].copy_(out, non_blocking=True)
 
     e2e_step()
-    stream.wait_stream(s_out)
     torch.cuda.synchronize()
     e_steps = max(1, min(args.steps, 5))
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    s_in.wait_stream(stream)
     for _ in range(e_steps):
         e2e_step()
-    stream.wait_stream(s_out)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b), world)
