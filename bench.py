@@ -85,29 +85,93 @@ def recorded_traffic(kernel_tag: str):
     return e.get("dram_bytes_per_launch")
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+# clocks-event reason bits of NVML's nvmlDeviceGetCurrentClocksEventReasons
+NVML_REASON_BITS = {"gpu_idle": 0x1, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
+                    "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
+NVML_CLOCK_SM = 1
 
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+def device_uuid(index: int):
+    """NVML-style UUID ("GPU-...") of CUDA device `index`, or None: CUDA and
+    NVML may number the GPUs differently, the UUID names the same one."""
+    try:
+        u = str(torch.cuda.get_device_properties(index).uuid)
+    except (AttributeError, RuntimeError):
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
+class ClockSampler:
+    """SM clock and throttle reasons of the GPU while the timed region runs.
+
+    NVML (through ctypes) is polled about every millisecond from a thread,
+    so even a timed region of a few milliseconds gets samples; samples that
+    NVML flags as idle are left out.  Without NVML, nvidia-smi polls every
+    100 ms instead."""
+
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
+        self.uuid = device_uuid(index)
         self.proc = None
+        self.thread = None
+        self.samples = []  # (sm MHz, reason bits) from NVML
+        self.lines = []    # nvidia-smi CSV lines
+        self.max_mhz = None
+
+    def _nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.uuid is None or lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+                return None
+            try:
+                reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+            except AttributeError:
+                reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            return lib, h, reasons
+        except (OSError, AttributeError):
+            return None
+
+    def _poll(self, lib, h, reasons):
+        import ctypes
+        clk, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(h, NVML_CLOCK_SM, ctypes.byref(clk)) == 0 and
+                    reasons(h, ctypes.byref(bits)) == 0):
+                self.samples.append((float(clk.value), int(bits.value)))
+            time.sleep(0.001)
 
     def __enter__(self):
+        import threading
+        nv = self._nvml()
+        if nv is not None:
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, args=nv, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", "-i", self.uuid or str(self.index),
+                 f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -118,24 +182,35 @@ class ClockSampler:
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[3:7]):
-                if v.lower() == "active":
-                    reasons.add(nm)
+        sm, mx, reasons = [], [], set()
+        if self.thread is not None:
+            busy = [(c, b) for c, b in self.samples if not b & NVML_REASON_BITS["gpu_idle"]]
+            for c, b in busy:
+                sm.append(c)
+                reasons.update(nm for nm in names if b & NVML_REASON_BITS[nm])
+            if self.max_mhz is not None:
+                mx.append(self.max_mhz)
+            source = "nvml"
+        else:
+            for ln in self.lines:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+            source = "nvidia-smi"
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": max(mx) if mx else None,
+                    "reasons": ["unsampled"], "samples": 0, "source": source}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "source": source}
 
 
 # --------------------------------------------------------------- workload --
