@@ -182,6 +182,42 @@ def test_topk_few_long_rows(rows, dtype, ld):
         assert_rows_equal(got, want, f"few long rows={rows} {dtype} k={k}")
 
 
+@pytest.mark.parametrize("rows,cols,dtype", [(700, 40000, torch.float32),
+                                             (64, 12000, torch.float32),
+                                             (64, 12000, torch.bfloat16)])
+def test_topk_sample_defeating_rows(rows, cols, dtype):
+    """Rows shaped against a sampled threshold, on the CTA-per-row paths
+    (700 x 40000: 256 threads per row; 64 x 12000: 128): a hidden block of
+    large values, a sparse periodic top, ramps both ways, a tie exactly at
+    the K-th value, a top block at the row's end, half the row -inf, and a
+    huge dynamic range.  Each must come out as the oracle's."""
+    x, _ = inputs.prefill(rows=rows, cols=cols, seed=cols + rows, dtype=torch.float32)
+    g = torch.Generator().manual_seed(rows + cols)
+    ends = torch.randint(0, cols + 1, (rows,), generator=g, dtype=torch.int32)
+    ends[:8] = cols
+    off = int(torch.randint(0, cols - 600, (1,), generator=g))
+    x[0, off:off + 600] = 10.0 + torch.rand(600, generator=g)      # hidden block
+    x[1, 7::61] = 5.0 + torch.rand(len(range(7, cols, 61)), generator=g)  # sparse period
+    x[2] = torch.arange(cols, dtype=torch.float32)                  # ascending ramp
+    x[3] = -torch.arange(cols, dtype=torch.float32)                 # descending ramp
+    x[4] = 1.0
+    x[4, torch.randperm(cols, generator=g)[:511]] = 3.0             # K-th value tied
+    x[5] = 1.0
+    x[5, cols - 513:] = 2.0                                         # top block at the end
+    x[6, : cols // 2] = float("-inf")
+    x[7] = x[7] * torch.where(torch.rand(cols, generator=g) < 0.5, 1e30, 1e-30)
+    x = x.to(dtype)
+    sample = sorted(set(range(12)) | set(np.random.default_rng(cols).integers(0, rows, 12).tolist()))
+    xd = x.to(DEV)
+    for k in (1, 512, 2048):
+        out = torch.full((rows, k + 3), CANARY, dtype=torch.int32, device=DEV)
+        satk.topk_rows(xd, k, row_ends=ends.to(DEV), out=out)
+        got = out.cpu().numpy()[sample]
+        want = np.full((len(sample), k + 3), CANARY, dtype=np.int32)
+        oracle.topk_rows(host_view(x[sample]), k, row_ends=ends[sample].numpy(), out=want)
+        assert_rows_equal(got, want, f"sample-defeating {rows}x{cols} {dtype} k={k}")
+
+
 def test_topk_decode_shaped_few_rows():
     """A handful of very long bf16 rows (the benchmark's 4 x 524288 case and
     shorter row ends), K = 384 and 2048."""
