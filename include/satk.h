@@ -96,8 +96,9 @@ int satk_topk_rows(const void *logits, int dtype, int64_t rows, int64_t cols,
 /*
  * satk_topk_rows_sorted -- satk_topk_rows with the chosen ids in score
  * order: descending score, ties by ascending column (a score-sorted output
- * option; the pages' selectors never sort, [P2 DCPTopkSelectKernel: "a
- * fixed order"]).  The chosen set, the -1 tail, the untouched columns
+ * option; the pages' selectors never sort, they emit in an order fixed by
+ * their thread layout [P2 DCPTopkSelectKernel]).  The chosen set, the -1
+ * tail, the untouched columns
  * [k, ld_out), the arguments and the errors are those of satk_topk_rows.
  * Slower: every row takes one CTA and a shared-memory sort of the k ids.
  */
