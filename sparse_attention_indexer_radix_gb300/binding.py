@@ -71,8 +71,18 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+# Stands in for the data pointer of a zero-size tensor (torch gives 0) in a
+# call whose batch is empty: the entry points check it is non-null and
+# aligned, then return before any launch, so it is never dereferenced.
+_EMPTY_BATCH_PTR = 256
+
+
+def _ptr(t, empty_batch: bool = False):
+    if t is None:
+        return None
+    if empty_batch and t.data_ptr() == 0:
+        return ctypes.c_void_p(_EMPTY_BATCH_PTR)
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(device):
@@ -125,7 +135,8 @@ def topk_rows(logits: torch.Tensor, k: int, row_ends: torch.Tensor | None = None
     ld = logits.stride(0) if rows > 1 else max(cols, 1)
     ld_out = out.stride(0) if rows > 1 else out.shape[1]
     f = lib().satk_topk_rows_sorted if sorted else lib().satk_topk_rows
-    rc = f(_ptr(logits), dt, rows, cols, ld, _ptr(row_ends), k, _ptr(out), ld_out,
+    e = rows == 0
+    rc = f(_ptr(logits, e), dt, rows, cols, ld, _ptr(row_ends, e), k, _ptr(out, e), ld_out,
            _stream(logits.device))
     _check(rc, "satk_topk_rows_sorted" if sorted else "satk_topk_rows")
     return out
@@ -163,8 +174,9 @@ def dcp_pack(logits: torch.Tensor, local_idx: torch.Tensor,
         raise SatkError(f"out must be contiguous int32 [{rows}, {packed_row_words(n)}]")
     ld = logits.stride(0) if rows > 1 else max(S, 1)
     ld_idx = local_idx.stride(0) if rows > 1 else n
-    rc = lib().satk_dcp_pack(_ptr(logits), rows, S, ld, _ptr(local_idx), ld_idx, n,
-                             _ptr(row_ends), _ptr(out), _stream(logits.device))
+    e = rows == 0
+    rc = lib().satk_dcp_pack(_ptr(logits, e), rows, S, ld, _ptr(local_idx, e), ld_idx, n,
+                             _ptr(row_ends, e), _ptr(out, e), _stream(logits.device))
     _check(rc, "satk_dcp_pack")
     return out
 
@@ -205,8 +217,9 @@ def dcp_merge_select(cand: torch.Tensor, k: int, *, packed: bool,
     if sat_word is not None and sat_word.numel() < T:
         raise SatkError("sat_word must hold T words")
     ld_out = ids_out.stride(0) if T > 1 else ids_out.shape[1]
-    rc = lib().satk_dcp_merge_select(_ptr(cand), fmt, W, T, n, k, _ptr(ids_out), ld_out,
-                                     _ptr(sat_word), _ptr(status), _stream(cand.device))
+    e = T == 0
+    rc = lib().satk_dcp_merge_select(_ptr(cand, e), fmt, W, T, n, k, _ptr(ids_out, e), ld_out,
+                                     _ptr(sat_word, e), _ptr(status), _stream(cand.device))
     _check(rc, "satk_dcp_merge_select")
     return ids_out
 
@@ -239,9 +252,10 @@ def dcp_rescue_select(packed: torch.Tensor, logits: torch.Tensor, sat_word: torc
         raise SatkError(f"recv must be contiguous int32 with >= {words_needed} words")
     _rowmajor_2d(ids_out, "ids_out")
     ld_out = ids_out.stride(0) if T > 1 else ids_out.shape[1]
-    rc = lib().satk_dcp_rescue_select(_ptr(packed), W, T, n, k, _ptr(logits), S, ld,
-                                      _ptr(row_ends), _ptr(sat_word), _ptr(recv),
-                                      _ptr(ids_out), ld_out, _ptr(status),
+    e = T == 0
+    rc = lib().satk_dcp_rescue_select(_ptr(packed, e), W, T, n, k, _ptr(logits, e), S, ld,
+                                      _ptr(row_ends, e), _ptr(sat_word, e), _ptr(recv, e),
+                                      _ptr(ids_out, e), ld_out, _ptr(status),
                                       _stream(packed.device))
     _check(rc, "satk_dcp_rescue_select")
     return recv
@@ -281,9 +295,10 @@ def dcp_emit_rows(ids: torch.Tensor, W: int, dcp_rank: int, req_id: torch.Tensor
     ld_ids = ids.stride(0) if T > 1 else ids.shape[1]
     ld_rows = rows_out.stride(0) if T > 1 else rows_out.shape[1]
     ld_table = block_table.stride(0) if R > 1 else max(width, 1)
-    rc = lib().satk_dcp_emit_rows(_ptr(ids), T, k, ld_ids, W, dcp_rank, _ptr(req_id),
-                                  _ptr(block_table), R, ld_table, max_blocks, block_size,
-                                  stride_rows, _ptr(rows_out), ld_rows, _ptr(valid_out),
+    e = T == 0
+    rc = lib().satk_dcp_emit_rows(_ptr(ids, e), T, k, ld_ids, W, dcp_rank, _ptr(req_id, e),
+                                  _ptr(block_table, e), R, ld_table, max_blocks, block_size,
+                                  stride_rows, _ptr(rows_out, e), ld_rows, _ptr(valid_out, e),
                                   _ptr(status), _stream(ids.device))
     _check(rc, "satk_dcp_emit_rows")
     return rows_out, valid_out

@@ -558,6 +558,34 @@ def test_abi_rejects_with_real_buffers():
     assert np.all(out.cpu().numpy() == 0)  # nothing was launched
 
 
+def test_empty_batches_are_no_ops():
+    """Zero rows (torch hands out a null data pointer for them): every entry
+    point returns at once with nothing written and nothing raised."""
+    W, n, k, S = 4, 64, 512, 1000
+    x = torch.empty((0, 5000), device=DEV)
+    assert satk.topk_rows(x, 512).shape == (0, 512)
+    assert satk.topk_rows(x, 512, row_ends=torch.empty(0, dtype=torch.int32, device=DEV),
+                          sorted=True).shape == (0, 512)
+    lg = torch.empty((0, S), dtype=torch.bfloat16, device=DEV)
+    local = torch.empty((0, n), dtype=torch.int32, device=DEV)
+    assert satk.dcp_pack(lg, local).shape == (0, n + n // 32)
+    packed = torch.empty((W, 0, n + n // 32), dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sat = torch.empty(0, dtype=torch.int32, device=DEV)
+    ids = satk.dcp_merge_select(packed, k, packed=True, sat_word=sat, status=status)
+    assert ids.shape == (0, k)
+    pairs = torch.empty((W, 0, 256, 2), dtype=torch.int32, device=DEV)
+    assert satk.dcp_merge_select(pairs, 256, packed=False).shape == (0, 256)
+    logits = torch.empty((W, 0, S), dtype=torch.bfloat16, device=DEV)
+    satk.dcp_rescue_select(packed, logits, sat, ids, k, status=status)
+    table = torch.zeros((3, 16), dtype=torch.int32, device=DEV)
+    rows, valid = satk.dcp_emit_rows(ids, W, 0, torch.empty(0, dtype=torch.int32, device=DEV),
+                                     table, 64, 64, status=status)
+    assert rows.shape == (0, k) and valid.shape == (0,)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
 # ------------------------------------------------------------- emit_rows --
 
 def run_emit_rows(ids, W, rank, req, table, B, stride, max_blocks=None, ld_rows=None):
