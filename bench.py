@@ -45,12 +45,25 @@ METRIC = "rows/s and achieved HBM GB/s (% of GB300 peak) for exact per-row top-K
 WORKLOAD = ("prefill top-K: 4096 query rows x {8192, 51200, 102400} cols fp32 ~N(0,1), "
             "K=512, causal row_end[i]=cols-4096+i+1, strided int32 output [4096, 640]")
 CPU_SAMPLE_STRIDE = 8  # every 8th row of each width: 512 rows per width
+# The prefill page's own times for this workload (vLLM PR #57206, Synthetic
+# controls): the native radix selector top_k_per_row_prefill on one GB200,
+# per width in microseconds.  Another machine's figure: context for
+# vs_baseline, not the target.
+PAGES_NATIVE_US = {8192: 80.9, 51200: 321.4, 102400: 688.3}
 
 
 def algorithmic_bytes(cols: int, rows: int = ROWS, k: int = K, elt: int = 4) -> int:
     """Valid prefixes read once plus the ids written once."""
     ends = np.clip(np.arange(rows) + (cols - rows + 1), 0, cols)
     return int(ends.sum()) * elt + rows * k * 4
+
+
+def pages_rows_per_s(widths=WIDTHS, rows=ROWS):
+    """rows/s of one step at the pages' per-width times, or None when the
+    step is not the pages' workload (a profiling subset)."""
+    if rows != ROWS or tuple(widths) != tuple(WIDTHS):
+        return None
+    return rows * len(widths) / (sum(PAGES_NATIVE_US[c] for c in widths) * 1e-6)
 
 
 def measured_peaks():
@@ -594,11 +607,17 @@ def run_gpu(args):
                              "rows_per_s": rows / (per_width_ms[jj] * 1e-3),
                              "gbs": gbs, "frac": gbs / peak, "alg_bytes": ab}
 
+    pages = pages_rows_per_s(widths, rows)
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None if pages is None else value / pages,
+        "baseline": None if pages is None else {
+            "value": pages, "unit": "rows/s",
+            "source": "prefill page (vLLM PR #57206, Synthetic controls): native "
+                      "top_k_per_row_prefill on one GB200, 80.9 + 321.4 + 688.3 us per step"},
+        "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "rows_per_step": rows_step, "k": K,
                    "l2": "inputs (2.55 GB per step) larger than L2; flush buffer before stages",
                    "parallelism": f"replicas x{world} (rows independent, no collective)"},

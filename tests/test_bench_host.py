@@ -70,3 +70,10 @@ def test_device_uuid_without_a_gpu_is_none():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert bench.device_uuid(0) is None
+
+
+def test_vs_baseline_reference_figure():
+    # 12288 rows over the pages' 80.9 + 321.4 + 688.3 us
+    assert bench.pages_rows_per_s() == pytest.approx(12288 / 1090.6e-6)
+    assert bench.pages_rows_per_s(widths=(8192,)) is None
+    assert bench.pages_rows_per_s(rows=1024) is None
