@@ -1,0 +1,135 @@
+"""Randomised pins of the oracle (hypothesis, CPU): rows of up to 160
+columns, any row end and any K, against a counting formulation that shares
+nothing with the oracle's sort -- a column is chosen exactly when fewer than
+K valid columns precede it under (score desc, column asc).  The same for the score-sorted layout and for the pairs merge
+(a candidate is chosen when fewer than K non-empty candidates precede it
+under (score desc, gid asc))."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+hypothesis = pytest.importorskip("hypothesis")
+from hypothesis import given, settings  # noqa: E402
+from hypothesis import strategies as st  # noqa: E402
+
+import oracle  # noqa: E402
+from checks import bf16_bits_to_f32, order_key  # noqa: E402
+
+SPECIALS = [math.nan, -math.inf, math.inf, -0.0, 0.0]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    oracle.build()
+
+
+def _values(draw, n):
+    """Scores with many ties (small integers), special values and reals."""
+    reals = st.floats(-1e30, 1e30, allow_nan=False).map(lambda v: float(np.float32(v)))
+    pool = st.one_of(st.sampled_from(SPECIALS), st.integers(-3, 3).map(float), reals)
+    return [draw(pool) for _ in range(n)]
+
+
+def _chosen(vals, end, k):
+    """Columns preceded by fewer than k valid columns, counted pairwise."""
+    valid = [c for c in range(end) if not math.isnan(vals[c])]
+    keys = {c: order_key(vals[c]) for c in valid}
+    out = []
+    for a in valid:
+        ahead = sum(1 for b in valid if keys[b] > keys[a] or (keys[b] == keys[a] and b < a))
+        if ahead < k:
+            out.append(a)
+    return out, keys, valid
+
+
+def _layout(vals, end, k):
+    chosen, keys, valid = _chosen(vals, end, k)
+    if len(valid) < k:
+        return sorted(chosen) + [-1] * (k - len(valid))
+    kth = min(keys[c] for c in chosen)
+    return (sorted(c for c in chosen if keys[c] > kth) +
+            sorted(c for c in chosen if keys[c] == kth))
+
+
+def _sorted_layout(vals, end, k):
+    chosen, keys, _ = _chosen(vals, end, k)
+    order = sorted(chosen, key=lambda c: (tuple(-v for v in keys[c]), c))
+    return order + [-1] * (k - len(order))
+
+
+@st.composite
+def topk_case(draw):
+    cols = draw(st.integers(1, 160))
+    rows = draw(st.integers(1, 4))
+    x = np.array([_values(draw, cols) for _ in range(rows)], dtype=np.float32)
+    ends = np.array([draw(st.integers(-3, cols + 3)) for _ in range(rows)], dtype=np.int32)
+    k = draw(st.integers(1, cols + 4))
+    return x, ends, k
+
+
+@settings(max_examples=150, deadline=None)
+@given(topk_case())
+def test_topk_rows_against_counting(case):
+    x, ends, k = case
+    got = oracle.topk_rows(x, k, row_ends=ends)
+    srt = oracle.topk_rows(x, k, row_ends=ends, sorted=True)
+    for i in range(len(x)):
+        e = max(0, min(int(ends[i]), x.shape[1]))
+        vals = x[i].tolist()
+        assert got[i].tolist() == _layout(vals, e, k)
+        assert srt[i].tolist() == _sorted_layout(vals, e, k)
+
+
+@settings(max_examples=100, deadline=None)
+@given(topk_case())
+def test_topk_rows_bf16_against_counting(case):
+    x, ends, k = case
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)  # truncate to bf16 patterns
+    got = oracle.topk_rows(bits, k, row_ends=ends)
+    vals = bf16_bits_to_f32(bits)
+    for i in range(len(x)):
+        e = max(0, min(int(ends[i]), x.shape[1]))
+        assert got[i].tolist() == _layout(vals[i].tolist(), e, k)
+
+
+@st.composite
+def pairs_case(draw):
+    W = draw(st.integers(1, 4))
+    T = draw(st.integers(1, 3))
+    n = draw(st.integers(1, 12))
+    k = draw(st.integers(1, W * n + 3))
+    scores = np.array([[_values(draw, n) for _ in range(T)] for _ in range(W)],
+                      dtype=np.float32)
+    gid = np.empty((W, T, n), dtype=np.int64)
+    for t in range(T):  # distinct gids per row, some negative (empty)
+        ids = draw(st.lists(st.integers(-2, 200), min_size=W * n, max_size=W * n,
+                            unique=True))
+        gid[:, t, :] = np.array(ids).reshape(W, n)
+    return scores, gid, k
+
+
+@settings(max_examples=150, deadline=None)
+@given(pairs_case())
+def test_pairs_merge_against_counting(case):
+    scores, gid, k = case
+    W, T, n = scores.shape
+    cand = np.empty((W, T, n, 2), dtype=np.int32)
+    cand[..., 0] = scores.view(np.int32)
+    cand[..., 1] = gid.astype(np.int32)
+    got = oracle.merge_pairs(cand, k)
+    for t in range(T):
+        ent = [(r * n + j, float(scores[r, t, j]), int(gid[r, t, j]))
+               for r in range(W) for j in range(n)
+               if gid[r, t, j] >= 0 and not math.isnan(scores[r, t, j])]
+        chosen = []
+        for f, s, g in ent:
+            ks = order_key(s)
+            ahead = sum(1 for _, s2, g2 in ent
+                        if order_key(s2) > ks or (order_key(s2) == ks and g2 < g))
+            if ahead < k:
+                chosen.append((f, g))
+        want = [g for _, g in sorted(chosen)] + [-1] * (k - len(chosen))
+        assert got[t].tolist() == want
