@@ -133,3 +133,54 @@ def test_pairs_merge_against_counting(case):
                 chosen.append((f, g))
         want = [g for _, g in sorted(chosen)] + [-1] * (k - len(chosen))
         assert got[t].tolist() == want
+
+
+@st.composite
+def decode_case(draw):
+    W = draw(st.integers(2, 4))
+    T = draw(st.integers(1, 3))
+    S = draw(st.integers(40, 400))
+    n = draw(st.sampled_from([32, 64]))
+    k = n * draw(st.integers(2, 4))
+    rng = np.random.default_rng(draw(st.integers(0, 2**31 - 1)))
+    levels = draw(st.sampled_from([0, 3, 40]))  # 0: bf16 of N(0,1); else few levels
+    if levels:
+        table = (rng.standard_normal(levels).astype(np.float32).view(np.uint32) >> 16)
+        bits = table[rng.integers(0, levels, size=(W, T, S))].astype(np.uint16)
+    else:
+        bits = (rng.standard_normal((W, T, S)).astype(np.float32).view(np.uint32)
+                >> 16).astype(np.uint16)
+    bits[rng.random((W, T, S)) < 0.02] = 0x7FC0                    # NaN
+    bits[rng.random((W, T, S)) < 0.01] = 0xFF80                    # -inf
+    for t in range(T):                                             # one skewed rank
+        if rng.random() < 0.6:
+            r = int(rng.integers(0, W))
+            pos = rng.choice(S, size=min(S, int(rng.integers(n, 2 * n + 1))), replace=False)
+            big = (3.0 + rng.random(len(pos))).astype(np.float32)
+            bits[r, t, pos] = (big.view(np.uint32) >> 16).astype(np.uint16)
+    ends = None
+    if draw(st.booleans()):
+        ends = rng.integers(0, S + 5, size=(W, T)).astype(np.int32)
+    return bits, n, k, ends
+
+
+@settings(max_examples=60, deadline=None)
+@given(decode_case())
+def test_decode_merge_exact_whenever_the_slots_suffice(case):
+    """The packed merge and its rescue, step by step in the oracle, end
+    with the top-k scores of the union of all ranks on every row, unless
+    more ranks saturated than there are rescue slots (status bit 0: the
+    row then keeps round 1)."""
+    from checks import check_decode_merge_row
+    bits, n, k, ends = case
+    W, T, S = bits.shape
+    flat = bits.reshape(W * T, S)
+    fe = None if ends is None else ends.reshape(-1)
+    local = oracle.topk_rows(flat, n, row_ends=fe)
+    packed = oracle.dcp_pack(flat, local, row_ends=fe).reshape(W, T, n + n // 32)
+    ids1, sat, st1 = oracle.merge_packed(packed, k)
+    ids2, _, st2 = oracle.rescue(packed, k, bits, sat, ids1.copy(), row_ends=ends)
+    hypothesis.assume(((st1 | st2) & 1) == 0)
+    assert (st1 | st2) == 0
+    for t in range(T):
+        check_decode_merge_row(ids2[t], bits, t, k, row_ends=ends)
