@@ -184,3 +184,52 @@ def test_decode_merge_exact_whenever_the_slots_suffice(case):
     assert (st1 | st2) == 0
     for t in range(T):
         check_decode_merge_row(ids2[t], bits, t, k, row_ends=ends)
+
+
+@st.composite
+def pack_case(draw):
+    rows = draw(st.integers(1, 4))
+    S = draw(st.sampled_from([50, 70000, 131072, 140000]))
+    n = draw(st.sampled_from([32, 64, 96]))
+    rng = np.random.default_rng(draw(st.integers(0, 2**31 - 1)))
+    bits = rng.integers(0, 1 << 16, size=(rows, S), dtype=np.int64).astype(np.uint16)
+    edges = np.array([-1, 0, 1, 65535, 65536, 65537, 131071, 131072, S - 1, S, S + 3])
+    local = np.where(rng.random((rows, n)) < 0.3, rng.choice(edges, size=(rows, n)),
+                     rng.integers(-2, S + 2, size=(rows, n))).astype(np.int32)
+    ends = None
+    if draw(st.booleans()):
+        ends = rng.integers(-1, S + 3, size=rows).astype(np.int32)
+    return bits, local, ends
+
+
+@settings(max_examples=80, deadline=None)
+@given(pack_case())
+def test_pack_words_decode_back(case):
+    """Each non-zero word gives back its slot's local id (low 16 bits
+    complemented, bit 16 from the plane) and score bits (the inverse of the
+    order-preserving ord16 map); zero words, with a clear plane bit, sit
+    exactly on the slots that cannot be packed (local outside [0, min(end,
+    S, 2**17)) or a NaN score)."""
+    bits, local, ends = case
+    rows, S = bits.shape
+    n = local.shape[1]
+    packed = oracle.dcp_pack(bits, local, row_ends=ends)
+    assert packed.shape == (rows, n + n // 32)
+    words = packed.view(np.uint32)
+    for i in range(rows):
+        lim = min(S, 1 << 17) if ends is None else min(max(int(ends[i]), 0), S, 1 << 17)
+        for j in range(n):
+            w = int(words[i, j])
+            plane = (int(words[i, n + j // 32]) >> (j % 32)) & 1
+            loc = int(local[i, j])
+            ok = 0 <= loc < lim
+            if ok:
+                h = int(bits[i, loc])
+                ok = not ((h & 0x7FFF) > 0x7F80)  # NaN
+            if not ok:
+                assert w == 0 and plane == 0, (i, j, loc)
+                continue
+            assert (0xFFFF - (w & 0xFFFF)) | (plane << 16) == loc
+            o = w >> 16
+            h_back = (o & 0x7FFF) if (o & 0x8000) else (~o & 0xFFFF)
+            assert h_back == int(bits[i, loc]), (i, j, hex(o), hex(int(bits[i, loc])))
