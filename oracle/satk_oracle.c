@@ -408,9 +408,10 @@ static int pcand_to_item(const pcand_t *pc, item_t *it) {
 
 static int decode_word(uint32_t word, uint32_t plane, int32_t j, int32_t owner,
                        int32_t W, pcand_t *out, int64_t flat) {
-  /* 0 is padding; a score field of 0 is the ord16 of a NaN pattern, which
-   * the pack never sends, so such a word is no candidate either */
-  if (word == 0 || (word >> 16) == 0) return 0;
+  /* [P2 _decode_key]: only the word 0 is padding.  Any other word is a
+   * candidate, a score field of 0 included: it ranks below every other
+   * score (the pack never sends one: 0 is the ord16 of a NaN pattern) */
+  if (word == 0) return 0;
   uint32_t local = (0xFFFFu - (word & 0xFFFFu)) |
                    (((plane >> (j % 32)) & 1u) << 16);
   out->ord = word >> 16;

@@ -484,3 +484,101 @@ def test_topk_sorted_is_the_unsorted_set():
             ids = b[i][b[i] >= 0]
             s = x[i, ids]
             assert np.all(s[:-1] >= s[1:])  # non-increasing scores
+
+
+# ------------------------------------------- hand-worked decode examples --
+
+def _load_golden_cases(name):
+    """Header keys (`key v ...`), `word r j hex` input words and `case K`
+    blocks (ids / sat / status) of a hand-worked merge example."""
+    head, words, cases = {}, [], []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *vals = line.split()
+        vals = [int(v, 0) for v in vals]
+        if key == "word":
+            words.append(vals)
+        elif key == "case":
+            cases.append({"K": vals[0]})
+        elif cases:
+            cases[-1][key] = vals if key == "ids" else vals[0]
+        else:
+            head[key] = vals if len(vals) > 1 else vals[0]
+    return head, words, cases
+
+
+def golden_packed_buffer(name):
+    """The [W, 1, N + N/32] B' buffer of a hand-worked example, and its cases."""
+    head, words, cases = _load_golden_cases(name)
+    W, n = head["W"], head["N"]
+    p = np.zeros((W, 1, n + n // 32), dtype=np.uint32)
+    for r, j, w in words:
+        p[r, 0, j] = w
+    return p.view(np.int32), cases
+
+
+def _u32(v):
+    return int(v) & 0xFFFFFFFF
+
+
+@pytest.mark.parametrize("name", ["decode_zero_score_example.txt",
+                                  "slots_exceeded_example.txt"])
+def test_packed_merge_hand_worked_examples(name):
+    """Words with a zero score field are candidates below every other score
+    (the page's _decode_key); a mask with more saturated ranks than slots,
+    which only repeated keys produce, is cleared with status bit 1."""
+    packed, cases = golden_packed_buffer(name)
+    for c in cases:
+        ids, sat, status = oracle.merge_packed(packed, c["K"])
+        assert ids[0].tolist() == c["ids"], (name, c["K"])
+        assert _u32(sat[0]) == c["sat"], (name, c["K"], hex(_u32(sat[0])))
+        assert status == c["status"], (name, c["K"], status)
+
+
+def load_rescue_plane_golden():
+    """Inputs and expected outputs of tests/golden/rescue_plane_example.txt:
+    logits bits [W, T, S] and a dict of the expected arrays."""
+    g = {}
+    cols = {}
+    for line in open(os.path.join(GOLDEN, "rescue_plane_example.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *vals = line.split()
+        vals = [int(v, 0) for v in vals]
+        if key == "cols":
+            cols[vals[0]] = (vals[1], vals[2:])
+        elif key in ("local", "packed"):
+            g.setdefault(key, {})[vals[0]] = vals[1:]
+        else:
+            g[key] = vals if len(vals) > 1 else vals[0]
+    W, T, S = g["W"], g["T"], g["S"]
+    bits = np.full((W, T, S), g["nan_bits"], dtype=np.uint16)
+    for r, (val, cs) in cols.items():
+        bits[r, 0, cs] = val
+    return bits, g
+
+
+def test_rescue_plane_hand_worked_example():
+    """Pushed local ids at and above 2**16 set their plane bits, a column at
+    2**17 is not pushed, and the re-select decodes the plane bits back into
+    distinct global ids (hand-worked table)."""
+    bits, g = load_rescue_plane_golden()
+    W, T, S, n, k = g["W"], g["T"], g["S"], g["N"], g["K"]
+    flat = bits.reshape(W * T, S)
+    local = oracle.topk_rows(flat, n)
+    for r in range(W):
+        assert local[r].tolist() == g["local"][r]
+    packed = oracle.dcp_pack(flat, local).reshape(W, T, n + n // 32)
+    for r in range(W):
+        assert [_u32(v) for v in packed[r, 0]] == g["packed"][r]
+    ids1, sat, st1 = oracle.merge_packed(packed, k)
+    assert ids1[0].tolist() == g["ids1"]
+    assert _u32(sat[0]) == g["sat"] and st1 == 0
+    ids2, recv, st2 = oracle.rescue(packed, k, bits, sat, ids1.copy())
+    assert [_u32(v) for v in recv[0, 0]] == g["recv"]
+    assert ids2[0].tolist() == g["ids2"]
+    assert st2 == g["status"]
+    assert len(set(g["ids2"])) == k  # the plane keeps the gids distinct
