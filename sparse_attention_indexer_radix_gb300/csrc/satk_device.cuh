@@ -286,7 +286,8 @@ struct Sel {
 };
 
 // Radix select over register keys: 11-bit digits from the top; KEYBITS 32
-// takes digits 11/11/10, KEYBITS 16 (bf16 keys, low half zero) 11/5.
+// takes digits 11/11/10, KEYBITS 16 (bf16 keys: low half zero, except the
+// key 1 of a zero score field) 11/5.
 template <int BLOCK, int KPT, int KEYBITS, bool AGG, class GetKey>
 __device__ Sel radix_select(GetKey gk, int K, SelectSmem<BLOCK> &sm) {
   Sel r;
@@ -329,7 +330,9 @@ __device__ Sel radix_select(GetKey gk, int K, SelectSmem<BLOCK> &sm) {
     p = reg_pass<BLOCK, KPT, 32, AGG>(gk, 16, prefix, 11, need, sm);
     need -= p.above;
     prefix = (prefix << 5) | (uint32_t)p.d;
-    r.T = prefix << 16;
+    // the score-0 digit holds only the key 1 (a B' word with a zero score
+    // field); T is that key, so that keys == T are exactly its ties
+    r.T = prefix == 0u ? 1u : prefix << 16;
     r.need = need;
     r.tie = p.cnt != need;
     return r;

@@ -67,8 +67,15 @@ __device__ MergeOut merge_core(const uint32_t (&keys)[KPT], GidOf gid, Out out, 
 }
 
 // B' word of slot j (plane word holds bit local[16] at j % 32) -> score key
-// (ord16 << 16, 0 for an empty word or a zero score field) and local id.
-__device__ __forceinline__ uint32_t bprime_key(uint32_t w) { return w & 0xffff0000u; }
+// and local id.  Only the word 0 is empty (vLLM API page
+// vllm.models.kimi_k3.nvidia.ops.dcp_topk_merge.kernels, _decode_key): a
+// non-zero word keys as ord16 << 16, or as 1 when its score field is 0 --
+// below every other score, above the empty key.  Every 16-bit select treats
+// 1 as the one key of score 0 (radix_select<..., 16> returns T = 1 for it).
+__device__ __forceinline__ uint32_t bprime_key(uint32_t w) {
+  const uint32_t k = w & 0xffff0000u;
+  return k != 0u ? k : (w != 0u ? 1u : 0u);
+}
 __device__ __forceinline__ uint32_t bprime_local(uint32_t w, uint32_t plane, int j) {
   return (0xffffu - (w & 0xffffu)) | (((plane >> (j & 31)) & 1u) << 16);
 }

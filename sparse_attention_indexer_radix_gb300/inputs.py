@@ -105,12 +105,12 @@ def pairs_merge(W: int = 8, rows: int = 6710, k: int = 2048, local: int = 16384,
 
 def decode_merge(W: int = 8, rows: int = 128, S: int = 65536, n: int = 384,
                  k: int = 2048, skew_frac: float = 0.25, skew_count: int = 600,
-                 seed: int = 1237, device="cpu"):
+                 seed: int = 1237, device="cpu", skew_from: int = 0):
     """bf16 logits [W, rows, S] ~ bf16(N(0,1)); on a seeded quarter of the
-    rows one seeded rank gets ``skew_count`` seeded positions set to
-    bf16(N(3.5, 0.25)), so that rank alone holds more than n of the row's
-    top-k.  Returns (logits, skewed_rows [bool rows], skew_rank [rows] (-1
-    where not skewed))."""
+    rows one seeded rank gets ``skew_count`` seeded positions (drawn from
+    columns [skew_from, S)) set to bf16(N(3.5, 0.25)), so that rank alone
+    holds more than n of the row's top-k.  Returns (logits, skewed_rows
+    [bool rows], skew_rank [rows] (-1 where not skewed))."""
     g = _gen(seed, device)
     lg = torch.randn((W, rows, S), generator=g, device=device).to(torch.bfloat16)
     n_skew = int(round(rows * skew_frac))
@@ -121,7 +121,7 @@ def decode_merge(W: int = 8, rows: int = 128, S: int = 65536, n: int = 384,
     for i in range(n_skew):
         t = int(skew_rows[i])
         r = int(ranks[i])
-        pos = torch.randperm(S, generator=g, device=device)[:skew_count]
+        pos = skew_from + torch.randperm(S - skew_from, generator=g, device=device)[:skew_count]
         vals = (torch.randn((skew_count,), generator=g, device=device) * 0.25 + 3.5)
         lg[r, t, pos] = vals.to(torch.bfloat16)
     skewed = skew_rank >= 0

@@ -6,7 +6,7 @@ both row paths (register-resident and streaming), fp32 and bf16, aligned and
 unaligned rows, the edge cases of the pages' test plans (empty and short
 rows, rows around K, full rows, strided output with untouched padding, -1
 tails, NaN rows, infinities, signed zeros, massive ties), and the workloads
-at their full sizes (sampled rows where the oracle would be slow)."""
+at their full sizes (every row)."""
 from __future__ import annotations
 
 import numpy as np
@@ -271,38 +271,44 @@ def test_adversarial_workload_full():
 
 
 @pytest.mark.parametrize("cols", inputs.PREFILL_COLS)
-def test_prefill_full_size_sampled(cols):
-    """The prefill workload at full size, in the launch configuration the
-    benchmark times; rows sampled for the oracle, properties on all rows."""
+def test_prefill_full_size_every_row(cols):
+    """The prefill workload at full size (4096 rows, K = 512, strided
+    output), in the launch configuration the benchmark times: every row
+    against the oracle, canaries past K intact."""
     x, ends = inputs.prefill(rows=inputs.PREFILL_ROWS, cols=cols, seed=1236, device=DEV)
-    check_full_size_sampled(x, ends, inputs.PREFILL_LD_OUT, seed=cols, what=f"prefill {cols}")
+    check_full_size(x, ends, inputs.PREFILL_LD_OUT, what=f"prefill {cols}")
 
 
 @pytest.mark.parametrize("rows,cols", [(8192, 4096), (8192, 8192), (2048, 25600), (2048, 51200),
                                        (1310, 102400)])
-def test_prefill_page_shapes_sampled(rows, cols):
-    """The other query-row x column shapes the benchmark reports, at full size."""
+def test_prefill_page_shapes_every_row(rows, cols):
+    """The other query-row x column shapes the benchmark reports, at full
+    size, every row against the oracle."""
     x, ends = inputs.prefill(rows=rows, cols=cols, seed=1250, device=DEV)
-    check_full_size_sampled(x, ends, inputs.PREFILL_K, seed=rows + cols, what=f"{rows}x{cols}")
+    check_full_size(x, ends, inputs.PREFILL_K, what=f"{rows}x{cols}")
 
 
 @pytest.mark.parametrize("mode", ["plus100", "times1e-8"])
-def test_prefill_shifted_full_size_sampled(mode):
-    """The distribution ablation the benchmark reports, 8192 x 8192, at full size."""
+def test_prefill_shifted_full_size_every_row(mode):
+    """The distribution ablation the benchmark reports, 8192 x 8192, at full
+    size, every row against the oracle."""
     x, ends = inputs.prefill_shifted(8192, 8192, mode, device=DEV)
-    check_full_size_sampled(x, ends, inputs.PREFILL_K, seed=7, what=mode)
+    check_full_size(x, ends, inputs.PREFILL_K, what=mode)
 
 
-def check_full_size_sampled(x, ends, ld_out, seed, what):
+def check_full_size(x, ends, ld_out, what, chunk=1024):
+    """Every row of a full-size launch against the oracle, canaries past K
+    included (the oracle runs in row chunks to bound host memory)."""
     rows, k = x.shape[0], inputs.PREFILL_K
     out = torch.full((rows, ld_out), CANARY, dtype=torch.int32, device=DEV)
     satk.topk_rows(x, k, row_ends=ends, out=out)
     got = out.cpu().numpy()
-    sample = np.unique(np.concatenate([[0, 1, rows - 1], np.random.default_rng(seed).integers(0, rows, 40)]))
-    xs = x[sample].cpu().numpy()
-    want = np.full((len(sample), ld_out), CANARY, dtype=np.int32)
-    oracle.topk_rows(xs, k, row_ends=ends[sample].cpu().numpy(), out=want)
-    assert_rows_equal(got[sample], want, f"{what} sampled")
+    ends_h = ends.cpu().numpy()
+    for r0 in range(0, rows, chunk):
+        r1 = min(rows, r0 + chunk)
+        want = np.full((r1 - r0, ld_out), CANARY, dtype=np.int32)
+        oracle.topk_rows(x[r0:r1].cpu().numpy(), k, row_ends=ends_h[r0:r1], out=want)
+        assert_rows_equal(got[r0:r1], want, f"{what} rows {r0}..{r1}")
     # every row (N(0,1): no NaN): min(end, k) ids in [0, end), unique, then
     # -1, canaries intact
     assert np.all(got[:, k:] == CANARY)
@@ -373,14 +379,40 @@ def test_pairs_merge_ties_empties_and_short_rows():
         assert_rows_equal(got, want, f"pairs ties k={kk}")
 
 
-def test_pairs_merge_full_size_sampled():
+def test_pairs_merge_full_size_every_row():
+    """The rank-major merge workload at full size (W = 8, 6710 rows, 8 x
+    2048 candidates per row, K = 2048): every row against the oracle."""
     W, R, k = 8, 6710, 2048
     cand = inputs.pairs_merge(W=W, rows=R, k=k, local=16384, seed=1236, device=DEV)
     got = satk.dcp_merge_select(cand, k, packed=False).cpu().numpy()
-    sample = np.unique(np.concatenate([[0, R - 1], np.random.default_rng(3).integers(0, R, 30)]))
-    cs = cand[:, sample].contiguous().cpu().numpy()
-    want = oracle.merge_pairs(cs, k)
-    assert_rows_equal(got[sample], want, "pairs full size sampled")
+    want = oracle.merge_pairs(cand.cpu().numpy(), k)
+    assert_rows_equal(got, want, "pairs full size")
+
+
+@pytest.mark.parametrize("k", [2049, 3000, 4096])
+def test_pairs_merge_k_above_2048(k):
+    """K above 2048 takes the wider list (8 warps x 1024 entries); 8 ranks
+    of 2048 candidates exceed it, so the sampled threshold runs too."""
+    W, R, n = 8, 24, 2048
+    cand = inputs.pairs_merge(W=W, rows=R, k=n, local=8192, seed=k, device=DEV)
+    got = satk.dcp_merge_select(cand, k, packed=False).cpu().numpy()
+    want = oracle.merge_pairs(cand.cpu().numpy(), k)
+    assert_rows_equal(got, want, f"pairs k={k}")
+
+
+@pytest.mark.parametrize("k", [512, 3000])
+def test_pairs_merge_16_byte_aligned_buffer(k):
+    """A pairs buffer that starts 16 bytes past a 32-byte boundary (two
+    pairs into an allocation) takes the 128-bit load path."""
+    W, R, n = 4, 20, 2048
+    cand = inputs.pairs_merge(W=W, rows=R, k=n, local=8192, seed=k + 1, device=DEV)
+    flat = torch.zeros(cand.numel() + 8, dtype=torch.int32, device=DEV)
+    view = flat[4:4 + cand.numel()].view(cand.shape)
+    view.copy_(cand)
+    assert view.data_ptr() % 32 == 16
+    got = satk.dcp_merge_select(view, k, packed=False).cpu().numpy()
+    want = oracle.merge_pairs(cand.cpu().numpy(), k)
+    assert_rows_equal(got, want, f"pairs 16-byte aligned k={k}")
 
 
 def _decode_gpu(lg, n, k, row_ends=None):
