@@ -457,59 +457,6 @@ __device__ __forceinline__ WarpDigit warp_find_digit(uint32_t *hist, int need) {
   return r;
 }
 
-// Outcome of a warp select (as Sel in satk_device.cuh).
-struct WarpSel {
-  uint32_t T;
-  int need;
-  bool tie, take_all;
-};
-
-// The K largest of the n keys key[0, n) (all non-zero), mn / mx their
-// smallest and largest: radix select with 8-bit digits cut from key - mn
-// over the bit-length of mx - mn.  With max_passes the passes may stop
-// early; T is then the start of the threshold digit (at least K keys >= T).
-__device__ __forceinline__ WarpSel warp_list_select(const uint32_t *key, int n, int K,
-                                                    uint32_t mn, uint32_t mx, uint32_t *hist,
-                                                    int max_passes) {
-  const int lane = lane_id();
-  WarpSel s{1u, 0, false, false};
-  if (n < K) {
-    s.take_all = true;
-    return s;
-  }
-  const uint32_t span = mx - mn;
-  const int b = span == 0u ? 0 : 32 - __clz(span);
-  int need = K;
-  uint32_t prefix = 0u;
-  int pbits = 0;
-  while (pbits < b) {
-    const int width = (b - pbits) < 8 ? (b - pbits) : 8;
-    const int shift = b - pbits - width;
-    const uint32_t dmask = (1u << width) - 1u;
-    for (int i = lane; i < n; i += 32) {
-      const uint32_t rel = key[i] - mn;
-      if (pbits == 0 || (rel >> (shift + width)) == prefix)
-        atomicAdd(hist + ((rel >> shift) & dmask), 1u);
-    }
-    __syncwarp();
-    const WarpDigit p = warp_find_digit(hist, need);
-    __syncwarp();
-    need -= p.above;
-    prefix = (prefix << width) | static_cast<uint32_t>(p.d);
-    pbits += width;
-    if (p.cnt == need || --max_passes == 0) {
-      s.T = mn + (prefix << shift);
-      s.need = need;
-      return s;
-    }
-  }
-  s.T = mn + prefix;  // every bit resolved: the K-th key, `need` of its ties wanted
-  s.need = need;
-  s.tie = true;
-  return s;
-}
-
-
 // ------------------------------------------------------- thresholds ------
 
 // The float whose ordered key is the smallest key >= T among the keys a
