@@ -385,9 +385,10 @@ def _stage_decode(dev, flush, peak, satk):
     req = torch.randperm(T, generator=g, device=dev).to(torch.int32)
     rows_out = torch.empty((T, k), dtype=torch.int32, device=dev)
     valid = torch.empty(T, dtype=torch.int32, device=dev)
+    # the step: the local top-N written straight as B' rows, the round-1
+    # merge with its saturation words, the rescue, this rank's KV rows
     parts = {
-        "local_topN": lambda: satk.topk_rows(flat, n, out=local),
-        "pack": lambda: satk.dcp_pack(flat, local, out=packed.view(W * T, -1)),
+        "topN_pack": lambda: satk.dcp_topk_pack(flat, n, out=packed.view(W * T, -1)),
         "merge_select": lambda: satk.dcp_merge_select(packed, k, packed=True, ids_out=ids,
                                                       sat_word=sat, status=status),
         "rescue": lambda: satk.dcp_rescue_select(packed, lg, sat, ids, k, recv=recv,
@@ -401,9 +402,32 @@ def _stage_decode(dev, flush, peak, satk):
             f()
         dec[name + "_us"] = timed_calls(f, 10, flush) * 1e3
     dec["total_us"] = sum(dec.values())
-    nb = flat.numel() * 2
-    dec["local_topN_gbs"] = nb / (dec["local_topN_us"] * 1e-6) / 1e9
-    dec["local_topN_frac"] = dec["local_topN_gbs"] / peak
+    # the same step replayed as one CUDA graph (launches back to back, L2
+    # flushed before each replay), as the pages time their kernels
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for f in parts.values():
+            f()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for f in parts.values():
+                f()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    dec["graph_us"] = timed_calls(graph.replay, 10, flush) * 1e3
+    # the two calls the fused one replaces, for reference (not in the totals)
+    ref = {"local_topN": lambda: satk.topk_rows(flat, n, out=local),
+           "pack": lambda: satk.dcp_pack(flat, local, out=packed.view(W * T, -1))}
+    for name, f in ref.items():
+        for _ in range(3):
+            f()
+        dec["unfused_" + name + "_us"] = timed_calls(f, 10, flush) * 1e3
+    nb = flat.numel() * 2 + packed.numel() * 4
+    dec["topN_pack_gbs"] = nb / (dec["topN_pack_us"] * 1e-6) / 1e9
+    dec["topN_pack_frac"] = dec["topN_pack_gbs"] / peak
     dec["saturated_rows"] = int(((sat >> 16) != 0).sum().item())
     st["decode_merge_W8_T128_S65536_N384_K2048"] = dec
     return st

@@ -130,6 +130,30 @@ int satk_dcp_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
                   satk_stream_t stream);
 
 /*
+ * satk_dcp_topk_pack -- each bf16 row's local top-n written straight as a B'
+ * row: the result of satk_dcp_pack applied to the ids satk_topk_rows(logits,
+ * n) returns, in one pass over the logits and without the ids or the
+ * gathered re-read of the scores [P2 DCPTopkPackKernel, dcp_topk_pack_indices;
+ * P3 Purpose for the row top-K].
+ *
+ * logits_bf16 : [rows, ld_logits] raw bfloat16, S valid columns; row i's
+ *               candidates are columns [0, min(row_ends[i], S)) (NULL row_ends:
+ *               S).  Columns >= end are never read.
+ * n           : a positive multiple of 32, at most SATK_TOPK_MAX_K.
+ * packed      : int32 [rows, n + n/32], contiguous.  Slot j holds the B' word
+ *               of the j-th id of the row's top-n layout (satk_topk_rows: the
+ *               ids above the n-th score ascending, then its ties), or 0 past
+ *               the last valid column or for a column >= 2**17; word n + j/32
+ *               holds that column's bit 16 at bit j % 32.
+ * Errors      : SATK_EINVAL for NULL pointers, rows < 0, S < 0, ld_logits < S,
+ *               n not a positive multiple of 32 or above SATK_TOPK_MAX_K,
+ *               S >= 2**31.
+ */
+int satk_dcp_topk_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
+                       int64_t ld_logits, const int32_t *row_ends, int32_t n,
+                       int32_t *packed, satk_stream_t stream);
+
+/*
  * satk_dcp_merge_select -- top-k over a rank-major candidate buffer read in
  * place [P1 Overview; P2 DCPTopkSelectKernel].
  *
@@ -290,6 +314,9 @@ int dcp_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
              int64_t ld_logits, const int32_t *local_idx, int64_t ld_idx,
              int32_t n, const int32_t *row_ends, int32_t *packed,
              satk_stream_t stream);
+int dcp_topk_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
+                  int64_t ld_logits, const int32_t *row_ends, int32_t n,
+                  int32_t *packed, satk_stream_t stream);
 int dcp_merge_select(const void *cand, int format, int32_t W, int64_t T,
                      int32_t n, int32_t k, int32_t *ids_out, int64_t ld_out,
                      int32_t *sat_word, int32_t *status, satk_stream_t stream);

@@ -28,7 +28,8 @@ MERGE_MAX_CANDIDATES = 32768
 EXPORTS = ("satk_topk_rows", "satk_dcp_pack", "satk_dcp_merge_select",
            "satk_dcp_rescue_select", "satk_rescue_recv_words", "satk_status_string",
            "satk_dcp_emit_rows", "satk_topk_rows_sorted", "topk_rows", "topk_rows_sorted",
-           "dcp_pack", "dcp_merge_select", "dcp_rescue_select", "dcp_emit_rows")
+           "dcp_pack", "dcp_merge_select", "dcp_rescue_select", "dcp_emit_rows",
+           "satk_dcp_topk_pack", "dcp_topk_pack")
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +54,7 @@ def lib() -> ctypes.CDLL:
                 "satk_topk_rows": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
                 "satk_topk_rows_sorted": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
                 "satk_dcp_pack": [vp, i64, i64, i64, vp, i64, i32, vp, vp, vp],
+                "satk_dcp_topk_pack": [vp, i64, i64, i64, vp, i32, vp, vp],
                 "satk_dcp_merge_select": [vp, c_int, i32, i64, i32, i32, vp, i64, vp, vp, vp],
                 "satk_dcp_rescue_select": [vp, i32, i64, i32, i32, vp, i64, i64, vp, vp, vp, vp,
                                            i64, vp, vp],
@@ -178,6 +180,31 @@ def dcp_pack(logits: torch.Tensor, local_idx: torch.Tensor,
     rc = lib().satk_dcp_pack(_ptr(logits, e), rows, S, ld, _ptr(local_idx, e), ld_idx, n,
                              _ptr(row_ends, e), _ptr(out, e), _stream(logits.device))
     _check(rc, "satk_dcp_pack")
+    return out
+
+
+def dcp_topk_pack(logits: torch.Tensor, n: int, row_ends: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    """The local top-n of each bf16 row of ``logits`` [rows, S] written
+    straight as B' rows ``out`` (int32 [rows, n + n/32], contiguous): what
+    dcp_pack makes of topk_rows(logits, n)."""
+    _need_cuda(logits, row_ends, out)
+    _rowmajor_2d(logits, "logits")
+    if logits.dtype != torch.bfloat16:
+        raise SatkError("dcp_topk_pack takes bfloat16 logits")
+    rows, S = logits.shape
+    if out is None:
+        out = torch.empty((rows, packed_row_words(n)), dtype=torch.int32, device=logits.device)
+    if out.dtype != torch.int32 or not out.is_contiguous() or \
+            out.numel() != rows * packed_row_words(n):
+        raise SatkError(f"out must be contiguous int32 [{rows}, {packed_row_words(n)}]")
+    if row_ends is not None and (row_ends.dtype != torch.int32 or not row_ends.is_contiguous()):
+        raise SatkError("row_ends must be contiguous int32")
+    ld = logits.stride(0) if rows > 1 else max(S, 1)
+    e = rows == 0
+    rc = lib().satk_dcp_topk_pack(_ptr(logits, e), rows, S, ld, _ptr(row_ends, e), n,
+                                  _ptr(out, e), _stream(logits.device))
+    _check(rc, "satk_dcp_topk_pack")
     return out
 
 

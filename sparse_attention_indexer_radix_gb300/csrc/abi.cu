@@ -79,3 +79,9 @@ extern "C" int dcp_rescue_select(const int32_t *packed, int32_t W, int64_t T, in
   return satk_dcp_rescue_select(packed, W, T, n, k, logits_bf16, S, ld_logits, row_ends,
                                 sat_word, recv, ids_out, ld_out, status, stream);
 }
+
+extern "C" int dcp_topk_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
+                             int64_t ld_logits, const int32_t *row_ends, int32_t n,
+                             int32_t *packed, satk_stream_t stream) {
+  return satk_dcp_topk_pack(logits_bf16, rows, S, ld_logits, row_ends, n, packed, stream);
+}

@@ -443,20 +443,22 @@ __device__ void warp_collect_exact(const T *__restrict__ xr, int end, int K, War
   __syncwarp();
 }
 
-// Select on the warp's key list and the ordered emit into o[0, K): 8-bit
+// Select on the warp's key list and the ordered emit (dst.put(pos, key,
+// column) for positions [0, K), dst.fill past the last candidate): 8-bit
 // digits relative to the list's key range; once the threshold digit holds
 // at most 32 keys they are ranked on the warp directly (each lane counts
 // the keys above and equal to its own) instead of more digit passes.
+template <class Out>
 __device__ __forceinline__ void warp_emit(WarpRowSmem &ws, const WarpRange &lr, int K,
-                                          int32_t *__restrict__ o) {
+                                          const Out &dst) {
   const int lane = lane_id();
   const unsigned lt = (1u << lane) - 1u;
   const uint32_t *lk = ws.key();
   const uint16_t *lc = ws.col();
   const int n = lr.n;
-  if (n < K) {  // fewer than K: every entry in list order, then -1
-    for (int i = lane; i < n; i += 32) o[i] = static_cast<int32_t>(lc[i]);
-    for (int q = n + lane; q < K; q += 32) o[q] = -1;
+  if (n < K) {  // fewer than K: every entry in list order, then the fill
+    for (int i = lane; i < n; i += 32) dst.put(i, lk[i], static_cast<int>(lc[i]));
+    for (int q = n + lane; q < K; q += 32) dst.fill(q);
     return;
   }
   const uint32_t mn = lr.mn;
@@ -536,10 +538,10 @@ __device__ __forceinline__ void warp_emit(WarpRowSmem &ws, const WarpRange &lr, 
     const uint32_t k = i < n ? lk[i] : 0u;
     const unsigned ba = __ballot_sync(kFull, k > v);
     const unsigned bb = __ballot_sync(kFull, k == v && i < n);
-    if ((ba >> lane) & 1u) o[runA + __popc(ba & lt)] = static_cast<int32_t>(lc[i]);
+    if ((ba >> lane) & 1u) dst.put(runA + __popc(ba & lt), k, static_cast<int>(lc[i]));
     if ((bb >> lane) & 1u) {
       const int pb = runB + __popc(bb & lt);
-      if (pb < takeB) o[cgt + pb] = static_cast<int32_t>(lc[i]);
+      if (pb < takeB) dst.put(cgt + pb, k, static_cast<int>(lc[i]));
     }
     runA += __popc(ba);
     runB += __popc(bb);
@@ -548,8 +550,8 @@ __device__ __forceinline__ void warp_emit(WarpRowSmem &ws, const WarpRange &lr, 
 
 // The whole row on one warp.  The histogram must be zero on entry and is
 // zero again on return.
-template <typename T, int ALIGN>
-__device__ void warp_topk_row(const T *__restrict__ xr, int end, int K, int32_t *__restrict__ o,
+template <typename T, int ALIGN, class Out>
+__device__ void warp_topk_row(const T *__restrict__ xr, int end, int K, const Out &dst,
                               WarpRowSmem &ws) {
   // the copy engine starts on the first batch of the filtered pass
   prefetch_groups<T, ALIGN>(xr, 0, min(end / 8, 32 * 4));
@@ -564,7 +566,7 @@ __device__ void warp_topk_row(const T *__restrict__ xr, int end, int K, int32_t 
     lr = warp_list_keys<T>(ws, n);
   else
     warp_collect_exact<T>(xr, end, K, ws, lr);
-  warp_emit(ws, lr, K, o);
+  warp_emit(ws, lr, K, dst);
 }
 
 }  // namespace satk

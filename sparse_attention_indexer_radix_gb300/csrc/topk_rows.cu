@@ -1,4 +1,5 @@
-// topk_rows.cu -- satk_topk_rows and satk_topk_rows_sorted: exact per-row
+// topk_rows.cu -- satk_topk_rows, satk_topk_rows_sorted and
+// satk_dcp_topk_pack: exact per-row
 // top-K over fp32 or bf16 logits with causal row ends, -1 padding and a
 // strided output ([Perf][DSA] Use DeepSelect for eligible sparse-indexer
 // prefill chunks, vLLM PR #57206: Purpose, Test Plan).
@@ -80,4 +81,19 @@ extern "C" int satk_topk_rows(const void *logits, int dtype, int64_t rows, int64
   if (row_alignment(x, ld_logits * 2) != 0)
     return topk_rows_launch_bf16_a16(x, rows, c, ld_logits, row_ends, k, out, ld_out, false, st);
   return topk_rows_launch_bf16_a0(x, rows, c, ld_logits, row_ends, k, out, ld_out, false, st);
+}
+
+extern "C" int satk_dcp_topk_pack(const uint16_t *logits_bf16, int64_t rows, int64_t S,
+                                  int64_t ld_logits, const int32_t *row_ends, int32_t n,
+                                  int32_t *packed, satk_stream_t stream) {
+  using namespace satk;
+  if (logits_bf16 == nullptr || packed == nullptr || rows < 0 || S < 0 || ld_logits < S ||
+      n < 32 || n % 32 != 0 || n > SATK_TOPK_MAX_K || S > INT_MAX || rows > INT_MAX)
+    return SATK_EINVAL;
+  if (rows == 0) return SATK_OK;
+  const cudaStream_t st = as_stream(stream);
+  const int c = static_cast<int>(S);
+  if (row_alignment(logits_bf16, ld_logits * 2) != 0)
+    return topk_pack_launch_bf16_a16(logits_bf16, rows, c, ld_logits, row_ends, n, packed, st);
+  return topk_pack_launch_bf16_a0(logits_bf16, rows, c, ld_logits, row_ends, n, packed, st);
 }

@@ -37,7 +37,43 @@ __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, 
   return e < 0 ? 0 : (e > cols ? cols : e);
 }
 
-template <typename T, int BLOCK, int SUB, int ALIGN>
+// Where a row's chosen candidates go: put(pos, key, column) for output
+// position pos of the row's top-K layout, fill(pos) past the last one;
+// start(t, nt) runs once per row, on threads t of nt, before any put.
+//  IdOut     -- the column ids, then -1 (satk_topk_rows).
+//  PackedOut -- the B' row of satk_dcp_topk_pack: word pos = the key's
+//               ord16 (bf16 keys are ord16 << 16) | (0xFFFF - column[15:0]),
+//               bit pos % 32 of word K + pos / 32 = column[16]; a column at
+//               or above 2**17 packs as 0, and so does every position past
+//               the last candidate (vLLM API page
+//               vllm.models.kimi_k3.nvidia.ops.dcp_topk_merge.kernels,
+//               DCPTopkPackKernel).  The plane words are zeroed in start and
+//               set with atomic ORs.
+struct IdOut {
+  int32_t *o;
+  int K;
+  __device__ __forceinline__ void start(int, int) const {}
+  __device__ __forceinline__ void put(int pos, uint32_t, int col) const { o[pos] = col; }
+  __device__ __forceinline__ void fill(int pos) const { o[pos] = -1; }
+};
+struct PackedOut {
+  int32_t *o;
+  int K;
+  __device__ __forceinline__ void start(int t, int nt) const {
+    for (int i = t; i < K / 32; i += nt) o[K + i] = 0;
+  }
+  __device__ __forceinline__ void put(int pos, uint32_t key, int col) const {
+    uint32_t w = 0u;
+    if (col < SATK_LOCAL_INDEX_LIMIT) {
+      w = (key & 0xffff0000u) | (0xffffu - (static_cast<uint32_t>(col) & 0xffffu));
+      if (col >> 16) atomicOr(o + K + pos / 32, 1 << (pos & 31));
+    }
+    o[pos] = static_cast<int32_t>(w);
+  }
+  __device__ __forceinline__ void fill(int pos) const { o[pos] = 0; }
+};
+
+template <typename T, int BLOCK, int SUB, int ALIGN, class Out = IdOut>
 __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) topk_rows_kernel(const T *__restrict__ x, int64_t ld,
                                                           int cols,
                                                           const int32_t *__restrict__ row_ends,
@@ -47,21 +83,22 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) topk_rows_kernel(const T 
   auto &sm = *reinterpret_cast<ListSmem<BLOCK, SUB> *>(smem_raw);
   const int64_t row = blockIdx.x;
   const int end = row_end_of(row_ends, row, cols);
+  const Out dst{out + row * ld_out, K};
+  dst.start(threadIdx.x, BLOCK);
   zero_hist(sm.sel);
   __syncthreads();
-  int32_t *o = out + row * ld_out;
   topk_row<T, BLOCK, SUB, ALIGN>(
       x + row * ld, end, K,
       [&](int pos, int i) {
-        if ((unsigned)pos < (unsigned)K) o[pos] = static_cast<int32_t>(sm.val[i]);
+        if ((unsigned)pos < (unsigned)K) dst.put(pos, sm.key[i], static_cast<int>(sm.val[i]));
       },
-      [&](int pos) { o[pos] = -1; }, sm);
+      [&](int pos) { dst.fill(pos); }, sm);
 }
 
-template <typename T, int BLOCK, int SUB, int ALIGN>
+template <typename T, int BLOCK, int SUB, int ALIGN, class Out = IdOut>
 int launch(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
            int32_t *out, int64_t ld_out, cudaStream_t st) {
-  auto kern = topk_rows_kernel<T, BLOCK, SUB, ALIGN>;
+  auto kern = topk_rows_kernel<T, BLOCK, SUB, ALIGN, Out>;
   const size_t smem = sizeof(ListSmem<BLOCK, SUB>);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   kern<<<dim3(static_cast<unsigned>(rows)), BLOCK, smem, st>>>(x, ld, cols, row_ends, K, out,
@@ -77,7 +114,7 @@ __host__ __device__ constexpr size_t sorted_buf_offset() {
 
 // Short rows: one warp per row (satk_warp.cuh), kWarpRowsPerCta rows per
 // CTA, seven CTAs per SM (their workspaces fill the shared memory).
-template <typename T, int ALIGN>
+template <typename T, int ALIGN, class Out = IdOut>
 __global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
     topk_rows_warp_kernel(const T *__restrict__ x, int64_t rows, int64_t ld, int cols,
                           const int32_t *__restrict__ row_ends, int K,
@@ -88,15 +125,16 @@ __global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
   if (row >= rows) return;  // warp-uniform; the warps never synchronise
   WarpRowSmem &ws = reinterpret_cast<WarpRowSmem *>(smem_raw)[warp];
   for (int i = lane_id(); i < 256; i += 32) ws.hist[i] = 0u;
+  const Out dst{out + row * ld_out, K};
+  dst.start(lane_id(), 32);
   __syncwarp();
-  warp_topk_row<T, ALIGN>(x + row * ld, row_end_of(row_ends, row, cols), K, out + row * ld_out,
-                          ws);
+  warp_topk_row<T, ALIGN>(x + row * ld, row_end_of(row_ends, row, cols), K, dst, ws);
 }
 
-template <typename T, int ALIGN>
+template <typename T, int ALIGN, class Out = IdOut>
 int launch_warp(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
-  auto kern = topk_rows_warp_kernel<T, ALIGN>;
+  auto kern = topk_rows_warp_kernel<T, ALIGN, Out>;
   const size_t smem = sizeof(WarpRowSmem) * kWarpRowsPerCta;
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   const int64_t grid = (rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta;
@@ -122,7 +160,7 @@ inline bool warp_rows_fit(int cols, int K) {
 // Few long rows: a cluster of C CTAs per row (satk_cluster.cuh); the grid
 // is rows x C, CTA blockIdx.x % C of the cluster taking slice
 // blockIdx.x % C of row blockIdx.x / C.
-template <typename T, int BLOCK, int SUB, int ALIGN, int C>
+template <typename T, int BLOCK, int SUB, int ALIGN, int C, class Out = IdOut>
 __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(BLOCK, 1024 / BLOCK)
     topk_rows_cluster_kernel(const T *__restrict__ x, int64_t ld, int cols,
                              const int32_t *__restrict__ row_ends, int K,
@@ -131,18 +169,20 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(BLOCK, 1024 / BLOCK)
   auto &cs = *reinterpret_cast<ClusterSmem<BLOCK, SUB> *>(smem_raw);
   cg::cluster_group cl = cg::this_cluster();
   const int64_t row = blockIdx.x / C;
+  const Out dst{out + row * ld_out, K};
+  if (cl.block_rank() == 0) dst.start(threadIdx.x, BLOCK);  // before the first cluster barrier
   zero_hist(cs.ls.sel);
   __syncthreads();
-  int32_t *o = out + row * ld_out;
   cluster_topk_row<T, BLOCK, SUB, ALIGN, C>(
       cl, x + row * ld, row_end_of(row_ends, row, cols), K,
-      [&](int pos, uint32_t, int col) { o[pos] = col; }, [&](int pos) { o[pos] = -1; }, cs);
+      [&](int pos, uint32_t key, int col) { dst.put(pos, key, col); },
+      [&](int pos) { dst.fill(pos); }, cs);
 }
 
-template <typename T, int BLOCK, int SUB, int ALIGN, int C>
+template <typename T, int BLOCK, int SUB, int ALIGN, int C, class Out = IdOut>
 int launch_cluster(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
                    int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
-  auto kern = topk_rows_cluster_kernel<T, BLOCK, SUB, ALIGN, C>;
+  auto kern = topk_rows_cluster_kernel<T, BLOCK, SUB, ALIGN, C, Out>;
   const size_t smem = sizeof(ClusterSmem<BLOCK, SUB>);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   kern<<<dim3(static_cast<unsigned>(rows * C)), BLOCK, smem, st>>>(x, ld, cols, row_ends, K,
@@ -178,37 +218,38 @@ int cluster_size(int64_t rows, int cols) {
   return c;
 }
 
-template <typename T, int BLOCK, int SUB, int ALIGN>
+template <typename T, int BLOCK, int SUB, int ALIGN, class Out = IdOut>
 int launch_rows_cta(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
                     int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
   switch (cluster_size<T, BLOCK, SUB, ALIGN>(rows, cols)) {
     case 2:
-      return launch_cluster<T, BLOCK, SUB, ALIGN, 2>(x, rows, cols, ld, row_ends, K, out, ld_out,
-                                                     st);
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 2, Out>(x, rows, cols, ld, row_ends, K, out,
+                                                          ld_out, st);
     case 4:
-      return launch_cluster<T, BLOCK, SUB, ALIGN, 4>(x, rows, cols, ld, row_ends, K, out, ld_out,
-                                                     st);
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 4, Out>(x, rows, cols, ld, row_ends, K, out,
+                                                          ld_out, st);
     case 8:
-      return launch_cluster<T, BLOCK, SUB, ALIGN, 8>(x, rows, cols, ld, row_ends, K, out, ld_out,
-                                                     st);
+      return launch_cluster<T, BLOCK, SUB, ALIGN, 8, Out>(x, rows, cols, ld, row_ends, K, out,
+                                                          ld_out, st);
     default:
-      return launch<T, BLOCK, SUB, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+      return launch<T, BLOCK, SUB, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
   }
 }
 
 // The list holds (BLOCK/32) warps x SUB candidates.
-template <typename T, int ALIGN>
+template <typename T, int ALIGN, class Out = IdOut>
 int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
   if (warp_rows_fit(cols, K))
-    return launch_warp<T, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+    return launch_warp<T, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
   if (cols <= kShortCols && K <= 512)
-    return launch<T, kShortBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+    return launch<T, kShortBlock, 512, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out, ld_out,
+                                                   st);
   if (K <= 1024)
-    return launch_rows_cta<T, kBlock, 512, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out,
-                                                  st);
-  return launch_rows_cta<T, kBlock, 1024, ALIGN>(x, rows, cols, ld, row_ends, K, out, ld_out,
-                                                 st);
+    return launch_rows_cta<T, kBlock, 512, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out,
+                                                       ld_out, st);
+  return launch_rows_cta<T, kBlock, 1024, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out,
+                                                      ld_out, st);
 }
 
 // ------------------------------------------------------- score-sorted --
@@ -309,5 +350,11 @@ int topk_rows_launch_bf16_a16(const uint16_t *x, int64_t rows, int cols, int64_t
 int topk_rows_launch_bf16_a0(const uint16_t *x, int64_t rows, int cols, int64_t ld,
                              const int32_t *row_ends, int K, int32_t *out, int64_t ld_out,
                              bool sorted, cudaStream_t st);
+// The local top-K of bf16 rows written as B' rows (PackedOut) of K + K/32
+// words: satk_dcp_topk_pack.
+int topk_pack_launch_bf16_a16(const uint16_t *x, int64_t rows, int cols, int64_t ld,
+                              const int32_t *row_ends, int K, int32_t *packed, cudaStream_t st);
+int topk_pack_launch_bf16_a0(const uint16_t *x, int64_t rows, int cols, int64_t ld,
+                             const int32_t *row_ends, int K, int32_t *packed, cudaStream_t st);
 
 }  // namespace satk

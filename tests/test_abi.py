@@ -43,7 +43,8 @@ def test_every_declared_function_is_exported(lib):
     names = declared_functions()
     assert {"satk_topk_rows", "satk_dcp_pack", "satk_dcp_merge_select",
             "satk_dcp_rescue_select", "satk_rescue_recv_words", "satk_status_string",
-            "topk_rows", "dcp_pack", "dcp_merge_select", "dcp_rescue_select"} <= set(names)
+            "topk_rows", "dcp_pack", "dcp_merge_select", "dcp_rescue_select",
+            "satk_dcp_topk_pack", "dcp_topk_pack"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} is declared in satk.h but not exported"
     assert set(binding.EXPORTS) <= set(names)
@@ -101,6 +102,26 @@ def test_pack_rejects(lib):
     assert call(n=0, ldi=0) == EINVAL
     assert call(ldi=63) == EINVAL
     assert call(ld=99) == EINVAL
+    assert call(rows=0) == 0
+
+
+@no_gpu
+def test_topk_pack_rejects(lib):
+    f = lib.satk_dcp_topk_pack
+    ok = dict(lg=P, rows=4, S=100, ld=100, re=NULL, n=64, out=P)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["lg"], a["rows"], a["S"], a["ld"], a["re"], a["n"], a["out"], NULL)
+    assert call(lg=NULL) == EINVAL
+    assert call(out=NULL) == EINVAL
+    assert call(rows=-1) == EINVAL
+    assert call(S=-1) == EINVAL
+    assert call(ld=99) == EINVAL
+    assert call(n=48) == EINVAL
+    assert call(n=0) == EINVAL
+    assert call(n=4096 + 32) == EINVAL
+    assert call(S=2**31, ld=2**31) == EINVAL
     assert call(rows=0) == 0
 
 

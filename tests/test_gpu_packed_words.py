@@ -236,3 +236,41 @@ def test_rescue_mask_bit_at_or_above_W():
     _assert_equal(g_ids.cpu().numpy(), w_ids, "ids")
     assert int(st.item()) == w_st and (w_st & 1)
     assert np.array_equal(w_ids[1:], ids[1:])
+
+
+# ------------------------------------------------ fused local top-n pack --
+
+@pytest.mark.parametrize("rows,S,n,ld_pad,ends", [
+    (40, 6000, 128, 0, True),        # one warp per row
+    (24, 40000, 384, 0, True),       # one CTA per row
+    (1024, 65536, 384, 0, False),    # the decode workload's local top-n
+    (6, 140000, 384, 0, True),       # few long rows (clusters), S above 2**17
+    (12, 20001, 256, 3, True),       # unaligned rows
+    (10, 3000, 2048, 0, False),      # n above the row length: zero words after
+])
+def test_topk_pack_matches_pack_of_topk(rows, S, n, ld_pad, ends):
+    """satk_dcp_topk_pack is dcp_pack(topk_rows(x, n)): every word and plane
+    word against the oracle's composition, on every row path (warp, CTA,
+    cluster), aligned and unaligned rows, row ends, NaN, ties, local ids at
+    and above 2**16 and 2**17."""
+    from sparse_attention_indexer_radix_gb300 import inputs
+    x, _ = inputs.prefill(rows=rows, cols=S, seed=S + n, causal=False, dtype=torch.bfloat16)
+    bits = _bits(x).copy()
+    bits[1, ::3] = 0x7FC0                          # NaN columns
+    bits[2, : S // 2] = 0x3F80                     # ties at 1.0
+    if S > (1 << 17):
+        bits[3, (1 << 17) - 5:(1 << 17) + 5] = 0x4300   # 128.0 around 2**17
+    re = None
+    if ends:
+        g = torch.Generator().manual_seed(S)
+        re = torch.randint(0, S + 10, (rows,), generator=g, dtype=torch.int32)
+        re[0] = S
+        re[4] = n // 2 if rows > 4 else re[4]
+    host = np.zeros((rows, S + ld_pad), dtype=np.uint16)
+    host[:, :S] = bits
+    buf = torch.from_numpy(host.view(np.int16)).view(torch.bfloat16).to(DEV)
+    got = satk.dcp_topk_pack(buf[:, :S], n, row_ends=None if re is None else re.to(DEV))
+    rn = None if re is None else re.numpy()
+    local = oracle.topk_rows(bits, n, row_ends=rn)
+    want = oracle.dcp_pack(bits, local, row_ends=rn)
+    _assert_equal(got.cpu().numpy(), want, f"topk_pack rows={rows} S={S} n={n}")
