@@ -299,6 +299,20 @@ int satk_dcp_emit_rows(const int32_t *ids, int64_t T, int32_t k, int64_t ld_ids,
                        int32_t *valid_out, int32_t *status,
                        satk_stream_t stream);
 
+/*
+ * satk_debug_flags -- the bounds-check bits of the debug build.  A library
+ * built with -DSATK_DEBUG (libsatk_debug.so) checks, inside its kernels,
+ * every shared-memory list index, output position, histogram bin and
+ * scratch index that the code relies on an invariant for; a failed check
+ * skips the access and ORs a bit into a device word (1 list index, 2 output
+ * position, 4 histogram bin, 8 scratch or plane-word index) instead of
+ * trapping.  This call waits for the device, returns the word and, when
+ * `clear` is non-zero, zeroes it; 0xffffffff if the device could not be
+ * read.  The normal build checks nothing and returns 0.  Not part of the
+ * pages' interface: a test aid of this library.
+ */
+uint32_t satk_debug_flags(int clear);
+
 /* A static, human-readable string for an SATK_* return code. */
 const char *satk_status_string(int rc);
 

@@ -8,6 +8,7 @@ without the compiled library every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -29,7 +30,7 @@ EXPORTS = ("satk_topk_rows", "satk_dcp_pack", "satk_dcp_merge_select",
            "satk_dcp_rescue_select", "satk_rescue_recv_words", "satk_status_string",
            "satk_dcp_emit_rows", "satk_topk_rows_sorted", "topk_rows", "topk_rows_sorted",
            "dcp_pack", "dcp_merge_select", "dcp_rescue_select", "dcp_emit_rows",
-           "satk_dcp_topk_pack", "dcp_topk_pack")
+           "satk_dcp_topk_pack", "dcp_topk_pack", "satk_debug_flags")
 
 _lock = threading.Lock()
 _lib = None
@@ -39,38 +40,65 @@ class SatkError(RuntimeError):
     pass
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Loads a build of the library at `path` and declares the signatures of
+    its entry points (include/satk.h)."""
+    if not os.path.exists(path):
+        raise SatkError(f"{path} is missing: build it with "
+                        "`python -m sparse_attention_indexer_radix_gb300.build`")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, c_int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
+    sigs = {
+        "satk_topk_rows": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
+        "satk_topk_rows_sorted": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
+        "satk_dcp_pack": [vp, i64, i64, i64, vp, i64, i32, vp, vp, vp],
+        "satk_dcp_topk_pack": [vp, i64, i64, i64, vp, i32, vp, vp],
+        "satk_dcp_merge_select": [vp, c_int, i32, i64, i32, i32, vp, i64, vp, vp, vp],
+        "satk_dcp_rescue_select": [vp, i32, i64, i32, i32, vp, i64, i64, vp, vp, vp, vp,
+                                   i64, vp, vp],
+        "satk_dcp_emit_rows": [vp, i64, i32, i64, i32, i32, vp, vp, i64, i64, i32, i32,
+                               i64, vp, i64, vp, vp, vp],
+    }
+    for name, args in sigs.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = c_int
+    L.satk_rescue_recv_words.argtypes = [i64, i32, i32]
+    L.satk_rescue_recv_words.restype = ctypes.c_size_t
+    L.satk_status_string.argtypes = [c_int]
+    L.satk_status_string.restype = ctypes.c_char_p
+    L.satk_debug_flags.argtypes = [c_int]
+    L.satk_debug_flags.restype = ctypes.c_uint
+    return L
+
+
+_routed = threading.local()
+
+
 def lib() -> ctypes.CDLL:
-    """The loaded library (raises if it has not been built)."""
+    """The library the calls of this module go to: libsatk.so, loaded on
+    first use (raises if it has not been built), or the one `routed_to`
+    selects for the current thread."""
     global _lib
+    r = getattr(_routed, "lib", None)
+    if r is not None:
+        return r
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise SatkError(
-                    f"{LIB_PATH} is missing: build it with "
-                    "`python -m sparse_attention_indexer_radix_gb300.build`")
-            L = ctypes.CDLL(LIB_PATH)
-            vp, i32, i64, c_int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
-            sigs = {
-                "satk_topk_rows": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
-                "satk_topk_rows_sorted": [vp, c_int, i64, i64, i64, vp, i32, vp, i64, vp],
-                "satk_dcp_pack": [vp, i64, i64, i64, vp, i64, i32, vp, vp, vp],
-                "satk_dcp_topk_pack": [vp, i64, i64, i64, vp, i32, vp, vp],
-                "satk_dcp_merge_select": [vp, c_int, i32, i64, i32, i32, vp, i64, vp, vp, vp],
-                "satk_dcp_rescue_select": [vp, i32, i64, i32, i32, vp, i64, i64, vp, vp, vp, vp,
-                                           i64, vp, vp],
-                "satk_dcp_emit_rows": [vp, i64, i32, i64, i32, i32, vp, vp, i64, i64, i32, i32,
-                                       i64, vp, i64, vp, vp, vp],
-            }
-            for name, args in sigs.items():
-                f = getattr(L, name)
-                f.argtypes = args
-                f.restype = c_int
-            L.satk_rescue_recv_words.argtypes = [i64, i32, i32]
-            L.satk_rescue_recv_words.restype = ctypes.c_size_t
-            L.satk_status_string.argtypes = [c_int]
-            L.satk_status_string.restype = ctypes.c_char_p
-            _lib = L
+            _lib = load(LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def routed_to(L: ctypes.CDLL):
+    """Within the block, this thread's calls go to the library L (another
+    build of the same sources, e.g. the bounds-checking debug build)."""
+    prev = getattr(_routed, "lib", None)
+    _routed.lib = L
+    try:
+        yield L
+    finally:
+        _routed.lib = prev
 
 
 # Stands in for the data pointer of a zero-size tensor (torch gives 0) in a

@@ -1,7 +1,13 @@
 """Builds libsatk.so in place: every .cu under csrc/ compiled for sm_103a in
 parallel, then linked into one shared library next to this file.
 
-    python -m sparse_attention_indexer_radix_gb300.build [--force]
+    python -m sparse_attention_indexer_radix_gb300.build [--force] [--debug]
+
+--debug builds libsatk_debug.so instead: the same sources with -DSATK_DEBUG,
+whose kernels check the bounds of their shared-memory list indices, output
+positions, histogram bins and scratch indices and record a failed check in
+a device word (satk_debug_flags) rather than trapping.  It is compiled as
+relocatable device code so that every translation unit shares that word.
 
 Object files go to _build/ (git-ignored); a source or header newer than the
 library triggers a rebuild.
@@ -21,6 +27,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "satk")
 LIB = os.path.join(HERE, "libsatk.so")
+BUILD_DEBUG = os.path.join(ROOT, "_build", "satk_debug")
+LIB_DEBUG = os.path.join(HERE, "libsatk_debug.so")
+DEBUG_FLAGS = ["-DSATK_DEBUG", "-rdc=true"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -43,23 +52,26 @@ def _deps():
         glob.glob(os.path.join(CSRC, "*.hpp")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    lib = LIB_DEBUG if debug else LIB
+    bdir = BUILD_DEBUG if debug else BUILD
+    extra = DEBUG_FLAGS if debug else []
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -69,14 +81,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = [nvcc, *ARCH, "-shared", *(["-rdc=true"] if debug else []), "-cudart", "static",
+           "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libsatk.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

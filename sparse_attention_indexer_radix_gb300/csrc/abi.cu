@@ -3,6 +3,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "satk_device.cuh"
 #include "satk_host.hpp"
 
 namespace satk {
@@ -28,6 +29,27 @@ int64_t resident_ctas(const void *kernel, int block, size_t smem) {
 }
 
 }  // namespace satk
+
+#ifdef SATK_DEBUG
+__device__ unsigned int satk::satk_debug_word;
+#endif
+
+extern "C" uint32_t satk_debug_flags(int clear) {
+#ifdef SATK_DEBUG
+  unsigned int h = 0u;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(&h, satk::satk_debug_word, sizeof h) != cudaSuccess)
+    return 0xffffffffu;
+  if (clear) {
+    const unsigned int z = 0u;
+    if (cudaMemcpyToSymbol(satk::satk_debug_word, &z, sizeof z) != cudaSuccess) return 0xffffffffu;
+  }
+  return h;
+#else
+  (void)clear;
+  return 0u;
+#endif
+}
 
 extern "C" const char *satk_status_string(int rc) {
   switch (rc) {

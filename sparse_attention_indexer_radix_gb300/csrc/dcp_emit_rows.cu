@@ -67,7 +67,10 @@ __global__ void __launch_bounds__(kEmitBlock) emit_rows_kernel(EmitArgs a) {
       par ^= 1;
 #pragma unroll
       for (int e = 0; e < kEmitPerThread; ++e)
-        if ((own >> e) & 1u) out[pos++] = phys[e];
+        if ((own >> e) & 1u) {
+          if (satk_check(pos < a.k, kDbgOut)) out[pos] = phys[e];
+          ++pos;
+        }
       n += total;
     }
   }

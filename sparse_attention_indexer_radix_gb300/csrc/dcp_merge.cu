@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(BLOCK) merge_select_kernel(
         }
       }
       keys[g] = key;
-      sm.gid[f] = gid;
+      if (satk_check(f < BLOCK * KPT, kDbgScratch)) sm.gid[f] = gid;
       j0 += 32;
       if (j0 >= n) {
         j0 -= n;
@@ -301,8 +301,10 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
             const int pos = pos0 + __popc(mm & ((1u << s) - 1u));
             if ((mm >> s) & 1u) {
               const uint32_t k = key_f32_num(grp[u].w[2 * s]);
-              lk[pos] = k;
-              lv[pos] = grp[u].w[2 * s + 1];
+              if (satk_check(pos < SUB, kDbgList)) {
+                lk[pos] = k;
+                lv[pos] = grp[u].w[2 * s + 1];
+              }
               kmn = min(kmn, k);
               kmx = max(kmx, k);
             }
@@ -445,8 +447,10 @@ __global__ void __launch_bounds__(kPackedBlock) packed_merge_list_kernel(
     const unsigned b = __ballot_sync(kFull, key != 0u);
     if (key != 0u) {
       const int pos = cnt + __popc(b & lt);
-      lk[pos] = key;
-      lv[pos] = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
+      if (satk_check(pos < SUB, kDbgList)) {
+        lk[pos] = key;
+        lv[pos] = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
+      }
       kmn = min(kmn, key);
       kmx = max(kmx, key);
     }

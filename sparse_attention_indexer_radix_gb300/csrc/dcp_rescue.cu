@@ -142,10 +142,14 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kPushBlock, 1024 / k
   cluster_topk_row<uint16_t, kPushBlock, SUB, ALIGN, C>(
       cl, logits + ((int64_t)r * T + t) * ld, static_cast<int>(end), K,
       [&](int pos, uint32_t key, int col) {
+        if (!satk_check(pos >= 0 && pos < K, kDbgOut)) return;
         dst[pos] = key | (0xffffu - (static_cast<uint32_t>(col) & 0xffffu));
         if ((col >> 16) & 1) atomicOr(dst + K + pos / 32, 1u << (pos & 31));
       },
-      [&](int pos) { dst[pos] = 0u; }, cs);
+      [&](int pos) {
+        if (satk_check(pos >= 0 && pos < K, kDbgOut)) dst[pos] = 0u;
+      },
+      cs);
 }
 
 template <int SUB, int ALIGN, int C>
@@ -207,7 +211,7 @@ __device__ void rescue_select_regs(RescueSmem<BLOCK, KPT> &sm, const int32_t *__
       }
     }
     keys[g] = key;
-    sm.gid[fb + lane] = gid;
+    if (satk_check(fb + lane < BLOCK * KPT, kDbgScratch)) sm.gid[fb + lane] = gid;
   }
   __syncthreads();
   const MergeOut m = merge_core<BLOCK, KPT, 16>(
@@ -284,8 +288,10 @@ __global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
     }
     if (key != 0u) {
       const int pos = cnt + __popc(b & lt);
-      lk[pos] = key;
-      lv[pos] = gid;
+      if (satk_check(pos < SUB, kDbgList)) {
+        lk[pos] = key;
+        lv[pos] = gid;
+      }
       kmn = min(kmn, key);
       kmx = max(kmx, key);
     }

@@ -28,6 +28,28 @@ namespace satk {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// ----------------------------------------------------------- debug checks --
+//
+// Built with -DSATK_DEBUG (libsatk_debug.so), device code checks the bound
+// of every shared-memory list index, output position, histogram bin and
+// scratch index that it relies on an invariant for, before the access: a
+// failed check skips the access and ORs a bit into the library's debug word
+// (read and cleared by satk_debug_flags), and never traps.  In the normal
+// build satk_check is the constant true and the checks compile away.
+constexpr unsigned kDbgList = 1u;     // a shared-memory list index
+constexpr unsigned kDbgOut = 2u;      // an output position
+constexpr unsigned kDbgHist = 4u;     // a histogram bin
+constexpr unsigned kDbgScratch = 8u;  // a scratch or plane-word index
+#ifdef SATK_DEBUG
+extern __device__ unsigned int satk_debug_word;
+__device__ __forceinline__ bool satk_check(bool ok, unsigned bit) {
+  if (!ok) atomicOr(&satk_debug_word, bit);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool satk_check(bool, unsigned) { return true; }
+#endif
+
 // ------------------------------------------------------------------ keys --
 
 __device__ __forceinline__ uint32_t key_f32(uint32_t b) {

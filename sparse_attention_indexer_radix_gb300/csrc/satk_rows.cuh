@@ -319,8 +319,10 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
         const int s = __ffs(mm) - 1;
         mm &= mm - 1u;
         const uint32_t k = key_of_num<T>(grp[u].raw(s));
-        lk[pos] = k;
-        lv[pos] = static_cast<uint32_t>(c0 + s);
+        if (satk_check(pos < SUB, kDbgList)) {
+          lk[pos] = k;
+          lv[pos] = static_cast<uint32_t>(c0 + s);
+        }
         kmn = min(kmn, k);
         kmx = max(kmx, k);
         ++pos;

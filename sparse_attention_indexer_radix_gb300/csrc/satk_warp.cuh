@@ -321,6 +321,8 @@ __device__ __forceinline__ bool warp_collect(const T *__restrict__ xr, int end, 
       uint32_t ak = static_cast<uint32_t>(__cvta_generic_to_shared(lk + pos));
       uint32_t ac = static_cast<uint32_t>(__cvta_generic_to_shared(lc + pos));
       const int c0 = (gb + u * 32 + lane) * 8;
+      const uint32_t mu = satk_check(pos + static_cast<int>(lcount) <= kWarpList, kDbgList)
+                              ? m[u] : 0u;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         asm volatile(
@@ -332,7 +334,7 @@ __device__ __forceinline__ bool warp_collect(const T *__restrict__ xr, int end, 
             "@p add.u32 %1, %1, 2;\n\t}"
             : "+r"(ak), "+r"(ac)
             : "r"(grp[u].raw(s)), "h"(static_cast<unsigned short>(c0 + s)),
-              "r"(m[u] & (1u << s))
+              "r"(mu & (1u << s))
             : "memory");
       }
       cnt += static_cast<int>((tot[u >> 1] >> (16 * (u & 1))) & 0xffffu);
@@ -429,7 +431,7 @@ __device__ void warp_collect_exact(const T *__restrict__ xr, int end, int K, War
     const unsigned bb = __ballot_sync(kFull, b);
     const bool keep = a || (b && runB + __popc(bb & lt) < need);
     const unsigned kb = __ballot_sync(kFull, keep);
-    if (keep) {
+    if (keep && satk_check(n + __popc(kb & lt) < kWarpList, kDbgList)) {
       const int pos = n + __popc(kb & lt);
       lk[pos] = k;
       lc[pos] = static_cast<uint16_t>(c);
@@ -493,7 +495,8 @@ __device__ __forceinline__ void warp_emit(WarpRowSmem &ws, const WarpRange &lr, 
         const uint32_t k = i < n ? lk[i] : 0u;
         const bool in = i < n && ((k - mn) >> shift) == prefix;
         const unsigned bb = __ballot_sync(kFull, in);
-        if (in) ws.hist[got + __popc(bb & lt)] = k;
+        if (in && satk_check(got + __popc(bb & lt) < 32, kDbgHist))
+          ws.hist[got + __popc(bb & lt)] = k;
         got += __popc(bb);
       }
       __syncwarp();

@@ -53,8 +53,12 @@ struct IdOut {
   int32_t *o;
   int K;
   __device__ __forceinline__ void start(int, int) const {}
-  __device__ __forceinline__ void put(int pos, uint32_t, int col) const { o[pos] = col; }
-  __device__ __forceinline__ void fill(int pos) const { o[pos] = -1; }
+  __device__ __forceinline__ void put(int pos, uint32_t, int col) const {
+    if (satk_check(pos >= 0 && pos < K, kDbgOut)) o[pos] = col;
+  }
+  __device__ __forceinline__ void fill(int pos) const {
+    if (satk_check(pos >= 0 && pos < K, kDbgOut)) o[pos] = -1;
+  }
 };
 struct PackedOut {
   int32_t *o;
@@ -63,6 +67,7 @@ struct PackedOut {
     for (int i = t; i < K / 32; i += nt) o[K + i] = 0;
   }
   __device__ __forceinline__ void put(int pos, uint32_t key, int col) const {
+    if (!satk_check(pos >= 0 && pos < K, kDbgOut)) return;
     uint32_t w = 0u;
     if (col < SATK_LOCAL_INDEX_LIMIT) {
       w = (key & 0xffff0000u) | (0xffffu - (static_cast<uint32_t>(col) & 0xffffu));
@@ -70,7 +75,9 @@ struct PackedOut {
     }
     o[pos] = static_cast<int32_t>(w);
   }
-  __device__ __forceinline__ void fill(int pos) const { o[pos] = 0; }
+  __device__ __forceinline__ void fill(int pos) const {
+    if (satk_check(pos >= 0 && pos < K, kDbgOut)) o[pos] = 0;
+  }
 };
 
 template <typename T, int BLOCK, int SUB, int ALIGN, class Out = IdOut>

@@ -22,6 +22,7 @@ import torch
 
 import oracle
 import sparse_attention_indexer_radix_gb300 as satk
+from guards import guarded
 from test_oracle_pins import golden_packed_buffer, load_rescue_plane_golden
 
 pytestmark = pytest.mark.gpu
@@ -52,10 +53,14 @@ def _assert_equal(got, want, what):
 
 
 def _merge_gpu(packed: np.ndarray, k: int):
-    sat = torch.full((packed.shape[1],), 77, dtype=torch.int32, device=DEV)
+    T = packed.shape[1]
+    sat, g_sat = guarded((T,), fill=77)
+    ids, g_ids = guarded((T, k))
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ids = satk.dcp_merge_select(torch.from_numpy(packed).to(DEV), k, packed=True,
-                                sat_word=sat, status=st)
+    satk.dcp_merge_select(torch.from_numpy(packed).to(DEV), k, packed=True, ids_out=ids,
+                          sat_word=sat, status=st)
+    g_sat("sat_word")
+    g_ids("ids")
     return ids.cpu().numpy(), sat.cpu().numpy(), int(st.item())
 
 
@@ -112,17 +117,28 @@ def _pipeline_gpu(lg_host: torch.Tensor, n: int, k: int, ld: int, row_ends=None)
     lg = buf[:, :, :S]
     flat = buf.view(W * T, ld)[:, :S]
     re = None if row_ends is None else row_ends.to(DEV)
-    local = satk.topk_rows(flat, n, row_ends=None if re is None else re.view(-1))
-    packed = satk.dcp_pack(flat, local, row_ends=None if re is None else re.view(-1)).view(
-        W, T, n + n // 32)
-    sat = torch.zeros(T, dtype=torch.int32, device=DEV)
+    local, g_local = guarded((W * T, n))
+    satk.topk_rows(flat, n, row_ends=None if re is None else re.view(-1), out=local)
+    packed, g_packed = guarded((W, T, n + n // 32))
+    satk.dcp_pack(flat, local, row_ends=None if re is None else re.view(-1),
+                  out=packed.view(W * T, n + n // 32))
+    fused, g_fused = guarded((W * T, n + n // 32))
+    satk.dcp_topk_pack(flat, n, row_ends=None if re is None else re.view(-1), out=fused)
+    sat, g_sat = guarded((T,), fill=0)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ids1 = satk.dcp_merge_select(packed, k, packed=True, sat_word=sat, status=st)
+    ids1, g_ids1 = guarded((T, k))
+    satk.dcp_merge_select(packed, k, packed=True, ids_out=ids1, sat_word=sat, status=st)
     slots = (k - 1) // n
-    recv = torch.full((T * slots * (k + k // 32),), 123, dtype=torch.int32, device=DEV)
-    ids2 = ids1.clone()
+    recv, g_recv = guarded((T * slots * (k + k // 32),), fill=123)
+    ids2, g_ids2 = guarded((T, k))
+    ids2.copy_(ids1)
     satk.dcp_rescue_select(packed, lg, sat, ids2, k, recv=recv, row_ends=re, status=st)
     torch.cuda.synchronize()
+    for chk, what in ((g_local, "local"), (g_packed, "packed"), (g_fused, "fused pack"),
+                      (g_sat, "sat_word"), (g_ids1, "round-1 ids"), (g_recv, "recv"),
+                      (g_ids2, "rescued ids")):
+        chk(what)
+    assert torch.equal(fused.view(W, T, -1), packed), "fused top-n pack differs from the pack"
     return dict(local=local.cpu().numpy(), packed=packed.cpu().numpy(), ids1=ids1.cpu().numpy(),
                 sat=sat.cpu().numpy(), ids2=ids2.cpu().numpy(),
                 recv=recv.cpu().numpy().reshape(T, slots, k + k // 32), status=int(st.item()))
@@ -269,7 +285,9 @@ def test_topk_pack_matches_pack_of_topk(rows, S, n, ld_pad, ends):
     host = np.zeros((rows, S + ld_pad), dtype=np.uint16)
     host[:, :S] = bits
     buf = torch.from_numpy(host.view(np.int16)).view(torch.bfloat16).to(DEV)
-    got = satk.dcp_topk_pack(buf[:, :S], n, row_ends=None if re is None else re.to(DEV))
+    got, guard = guarded((rows, n + n // 32))
+    satk.dcp_topk_pack(buf[:, :S], n, row_ends=None if re is None else re.to(DEV), out=got)
+    guard("topk_pack out")
     rn = None if re is None else re.numpy()
     local = oracle.topk_rows(bits, n, row_ends=rn)
     want = oracle.dcp_pack(bits, local, row_ends=rn)

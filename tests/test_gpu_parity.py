@@ -16,6 +16,7 @@ import torch
 import oracle
 import sparse_attention_indexer_radix_gb300 as satk
 from checks import check_decode_merge_row, check_topk_layout, check_topk_row, packed_contract
+from guards import guarded
 from sparse_attention_indexer_radix_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
@@ -49,8 +50,9 @@ def run_topk(x: torch.Tensor, k: int, ends: torch.Tensor | None, ld_out: int, ld
         xg = buf[:, :cols]
     else:
         xg = x.to(DEV)
-    out = torch.full((rows, ld_out), CANARY, dtype=torch.int32, device=DEV)
+    out, guard = guarded((rows, ld_out), fill=CANARY)
     satk.topk_rows(xg, k, row_ends=None if ends is None else ends.to(DEV), out=out, sorted=sorted)
+    guard("topk_rows out")
     want = np.full((rows, ld_out), CANARY, dtype=np.int32)
     oracle.topk_rows(host_view(x), k, row_ends=None if ends is None else ends.numpy(), out=want,
                      sorted=sorted)
@@ -384,7 +386,10 @@ def test_pairs_merge_full_size_every_row():
     2048 candidates per row, K = 2048): every row against the oracle."""
     W, R, k = 8, 6710, 2048
     cand = inputs.pairs_merge(W=W, rows=R, k=k, local=16384, seed=1236, device=DEV)
-    got = satk.dcp_merge_select(cand, k, packed=False).cpu().numpy()
+    ids, guard = guarded((R, k))
+    satk.dcp_merge_select(cand, k, packed=False, ids_out=ids)
+    guard("pairs ids")
+    got = ids.cpu().numpy()
     want = oracle.merge_pairs(cand.cpu().numpy(), k)
     assert_rows_equal(got, want, "pairs full size")
 
@@ -419,17 +424,24 @@ def _decode_gpu(lg, n, k, row_ends=None):
     W, T, S = lg.shape
     g = lg.to(DEV)
     re = None if row_ends is None else row_ends.to(DEV)
-    local = satk.topk_rows(g.view(W * T, S), n, row_ends=None if re is None else re.view(-1))
-    packed = satk.dcp_pack(g.view(W * T, S), local,
-                           row_ends=None if re is None else re.view(-1)).view(W, T, n + n // 32)
-    sat = torch.zeros(T, dtype=torch.int32, device=DEV)
+    local, g_local = guarded((W * T, n))
+    satk.topk_rows(g.view(W * T, S), n, row_ends=None if re is None else re.view(-1), out=local)
+    packed, g_packed = guarded((W, T, n + n // 32))
+    satk.dcp_pack(g.view(W * T, S), local, row_ends=None if re is None else re.view(-1),
+                  out=packed.view(W * T, n + n // 32))
+    sat, g_sat = guarded((T,), fill=0)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ids1 = satk.dcp_merge_select(packed, k, packed=True, sat_word=sat, status=status)
+    ids1, g_ids1 = guarded((T, k))
+    satk.dcp_merge_select(packed, k, packed=True, ids_out=ids1, sat_word=sat, status=status)
     slots = (k - 1) // n
-    recv = torch.full((T * slots * (k + k // 32),), 123, dtype=torch.int32, device=DEV)
-    ids2 = ids1.clone()
+    recv, g_recv = guarded((T * slots * (k + k // 32),), fill=123)
+    ids2, g_ids2 = guarded((T, k))
+    ids2.copy_(ids1)
     satk.dcp_rescue_select(packed, g, sat, ids2, k, recv=recv, row_ends=re, status=status)
     torch.cuda.synchronize()
+    for chk, what in ((g_local, "local"), (g_packed, "packed"), (g_sat, "sat_word"),
+                      (g_ids1, "round-1 ids"), (g_recv, "recv"), (g_ids2, "rescued ids")):
+        chk(what)
     return dict(local=local.cpu().numpy(), packed=packed.cpu().numpy(), ids1=ids1.cpu().numpy(),
                 sat=sat.cpu().numpy(), ids2=ids2.cpu().numpy(),
                 recv=recv.cpu().numpy().reshape(T, slots, k + k // 32),
@@ -624,13 +636,15 @@ def run_emit_rows(ids, W, rank, req, table, B, stride, max_blocks=None, ld_rows=
     """GPU (through the C ABI) and oracle outputs for host int32 arrays."""
     T, k = ids.shape
     ld_rows = k if ld_rows is None else ld_rows
-    rows = torch.full((T, ld_rows), CANARY, dtype=torch.int32, device=DEV)
-    valid = torch.full((T,), CANARY, dtype=torch.int32, device=DEV)
+    rows, g_rows = guarded((T, ld_rows), fill=CANARY)
+    valid, g_valid = guarded((T,), fill=CANARY)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     satk.dcp_emit_rows(torch.from_numpy(ids).to(DEV), W, rank, torch.from_numpy(req).to(DEV),
                        torch.from_numpy(table).to(DEV), B, stride, max_blocks=max_blocks,
                        rows_out=rows[:, :k] if ld_rows != k else rows, valid_out=valid,
                        status=st)
+    g_rows("rows_out")
+    g_valid("valid_out")
     want_rows, want_valid, want_st = oracle.emit_rows(ids, W, rank, req, table, B, stride,
                                                       max_blocks=max_blocks, ld_rows=ld_rows)
     return (rows.cpu().numpy(), valid.cpu().numpy(), int(st.item())), \
