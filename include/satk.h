@@ -244,9 +244,12 @@ size_t satk_rescue_recv_words(int64_t T, int32_t n, int32_t k);
  * rejected with SATK_EUNSUPPORTED before anything is launched.
  *
  * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and keeps it; make
- *   that first call before any stream capture.  A failed look-up returns
- *   SATK_ECUDA.
+ *   (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *   rest of the process; make that first call before any stream capture.
+ *   A failed look-up returns SATK_ECUDA.  Resetting the device after that
+ *   (cudaDeviceReset, or anything else that destroys its primary context)
+ *   is not supported: the array moves when the library's module is loaded
+ *   again, and the kept address would be stale.
  * - Every call on a device uses the same array and leaves its contents
  *   behind.  Nothing in it needs to start at zero: each slot a call reads
  *   is written by that same call first.  Calls that can run at the same

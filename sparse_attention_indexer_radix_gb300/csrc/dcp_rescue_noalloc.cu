@@ -13,7 +13,10 @@
 // name as a device address (on the host the name only stands for a shadow
 // object), so the address is looked up with cudaGetSymbolAddress once per
 // device, with that device current, on the first call made on that device,
-// and then passed to the kernels like any caller-owned buffer.
+// and then passed to the kernels like any caller-owned buffer.  The kept
+// address is valid as long as the device's primary context lives: a device
+// reset after the first call is not supported (the module, and with it the
+// array, would be loaded again at another address).
 #include <climits>
 #include <mutex>
 
