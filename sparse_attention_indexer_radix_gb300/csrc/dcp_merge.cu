@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kPackedBlock) packed_merge_list_kernel(
     const int32_t *row = cand + ((int64_t)r * T + t) * words;
     const uint32_t w = static_cast<uint32_t>(__ldg(row + j));
     const uint32_t plane = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
-    const uint32_t key = bprime_key(w);
+    const uint32_t key = bprime_list_key(w);
     const unsigned b = __ballot_sync(kFull, key != 0u);
     if (key != 0u) {
       const int pos = cnt + __popc(b & lt);
@@ -468,10 +468,10 @@ __global__ void __launch_bounds__(kPackedBlock) packed_merge_list_kernel(
       st);
   int bits = m.dup ? SATK_STATUS_DUPLICATE_KEYS : 0;
   if (sat_word != nullptr) {
-    const uint32_t tau = (m.nsel == K) ? (m.kmin >> 16) : 0u;
+    const uint32_t tau = (m.nsel == K) ? (m.kmin - 1u) : 0u;  // list keys are ord16 + 1
     for (int j = 0; j < sg.rounds(); ++j) {
       const int i = j * 32 + lane;
-      if (i < sg.cnt && (sm.key[sg.base + i] >> 16) > tau)
+      if (i < sg.cnt && sm.key[sg.base + i] > tau + 1u)
         atomicAdd(&above[sm.val[sg.base + i] % static_cast<uint32_t>(W)], 1);
     }
     __syncthreads();

@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
         const int32_t *row = packed + ((int64_t)r * T + t) * words_r1;
         const uint32_t w = static_cast<uint32_t>(__ldg(row + j));
         const uint32_t plane = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
-        key = bprime_key(w);
+        key = bprime_list_key(w);
         gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
       }
     } else {
@@ -277,10 +277,10 @@ __global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
       const int32_t *sl = recv + ((int64_t)t * slots + s) * words_k;
       const uint32_t w = static_cast<uint32_t>(sl[j]);
       const uint32_t plane = static_cast<uint32_t>(sl[K + ((j - lane) >> 5)]);
-      key = bprime_key(w);
+      key = bprime_list_key(w);
       gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)nth_set_bit(mask, s);
     }
-    if ((key >> 16) < tau) key = 0u;  // below the round-1 cut (or empty)
+    if (key <= tau) key = 0u;  // ord16 below the round-1 cut (or empty); keys are ord16 + 1
     const unsigned b = __ballot_sync(kFull, key != 0u);
     if (cnt + __popc(b) > SUB) {  // warp-uniform
       if (lane == 0) sm.flag = 1;

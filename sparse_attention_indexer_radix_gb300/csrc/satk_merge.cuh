@@ -76,6 +76,14 @@ __device__ __forceinline__ uint32_t bprime_key(uint32_t w) {
   const uint32_t k = w & 0xffff0000u;
   return k != 0u ? k : (w != 0u ? 1u : 0u);
 }
+// The same word's key in the shared-memory list engine: ord16 + 1 (0 for
+// the empty word only), so that the list select's range-relative digits
+// cover the score's 16 bits and nothing else (ord16 << 16 would leave 16
+// bits that are always zero, and every key of their digit passes would
+// land in one histogram bin).  Order is that of bprime_key.
+__device__ __forceinline__ uint32_t bprime_list_key(uint32_t w) {
+  return w == 0u ? 0u : (w >> 16) + 1u;
+}
 __device__ __forceinline__ uint32_t bprime_local(uint32_t w, uint32_t plane, int j) {
   return (0xffffu - (w & 0xffffu)) | (((plane >> (j & 31)) & 1u) << 16);
 }
