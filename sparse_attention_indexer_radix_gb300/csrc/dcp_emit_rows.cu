@@ -29,6 +29,8 @@ struct EmitArgs {
   int32_t *rows_out;
   int64_t ld_rows;
   int32_t *valid_out, *status;
+  int w_shift, b_shift;  // log2 of W and block_size when powers of two, else -1
+  bool vec_ids;          // every row of ids starts 16-byte aligned
 };
 
 __global__ void __launch_bounds__(kEmitBlock) emit_rows_kernel(EmitArgs a) {
@@ -45,18 +47,29 @@ __global__ void __launch_bounds__(kEmitBlock) emit_rows_kernel(EmitArgs a) {
     for (int base = 0; base < a.k; base += kEmitBlock * kEmitPerThread) {
       const int j0 = base + static_cast<int>(threadIdx.x) * kEmitPerThread;
       int32_t phys[kEmitPerThread];
+      int g8[kEmitPerThread];
       unsigned own = 0u;
+      if (a.vec_ids && j0 + kEmitPerThread <= a.k) {  // two 16-byte loads
+        const int4 u = __ldg(reinterpret_cast<const int4 *>(id + j0));
+        const int4 v = __ldg(reinterpret_cast<const int4 *>(id + j0) + 1);
+        g8[0] = u.x; g8[1] = u.y; g8[2] = u.z; g8[3] = u.w;
+        g8[4] = v.x; g8[5] = v.y; g8[6] = v.z; g8[7] = v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < kEmitPerThread; ++e) g8[e] = j0 + e < a.k ? id[j0 + e] : -1;
+      }
 #pragma unroll
       for (int e = 0; e < kEmitPerThread; ++e) {
-        const int j = j0 + e;
-        const int g = j < a.k ? id[j] : -1;
+        const int g = g8[e];
         phys[e] = 0;
-        if (g >= 0 && g % a.W == a.rank) {
-          const int local = g / a.W;
-          const int b = local / a.block_size;
+        const int owner = a.w_shift >= 0 ? (g & ((1 << a.w_shift) - 1)) : g % a.W;
+        if (g >= 0 && owner == a.rank) {
+          const int local = a.w_shift >= 0 ? (g >> a.w_shift) : g / a.W;
+          const int b = a.b_shift >= 0 ? (local >> a.b_shift) : local / a.block_size;
+          const int in_block = a.b_shift >= 0 ? (local & ((1 << a.b_shift) - 1))
+                                              : local % a.block_size;
           if (b < a.max_blocks) {
-            const int64_t p = static_cast<int64_t>(table[b]) * a.stride_rows +
-                              local % a.block_size;
+            const int64_t p = static_cast<int64_t>(table[b]) * a.stride_rows + in_block;
             phys[e] = static_cast<int32_t>(static_cast<uint32_t>(static_cast<uint64_t>(p)));
             own |= 1u << e;
           }
@@ -98,9 +111,17 @@ extern "C" int satk_dcp_emit_rows(const int32_t *ids, int64_t T, int32_t k, int6
       block_size < 1 || ld_rows_out < k || T > INT32_MAX)
     return SATK_EINVAL;
   if (T == 0) return SATK_OK;
+  auto log2_or = [](int v) {
+    if (v <= 0 || (v & (v - 1)) != 0) return -1;
+    int s = 0;
+    while ((1 << s) < v) ++s;
+    return s;
+  };
+  const bool vec_ids = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0 && ld_ids % 4 == 0;
   EmitArgs a{ids,        T,           ld_ids,     k,           W,         dcp_rank,
              req_id,     block_table, table_rows, ld_block_table, max_blocks, block_size,
-             stride_rows, rows_out,   ld_rows_out, valid_out,  status};
+             stride_rows, rows_out,   ld_rows_out, valid_out,  status,
+             log2_or(W), log2_or(block_size), vec_ids};
   emit_rows_kernel<<<dim3(static_cast<unsigned>(T)), kEmitBlock, 0, as_stream(stream)>>>(a);
   return launch_status();
 }

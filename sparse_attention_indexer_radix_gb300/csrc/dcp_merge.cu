@@ -437,24 +437,46 @@ __global__ void __launch_bounds__(kPackedBlock) packed_merge_list_kernel(
   uint32_t *lv = sm.val + warp * SUB;
   int cnt = 0;
   uint32_t kmn = 0xffffffffu, kmx = 0u;
-  for (int c = c0; c < c1; ++c) {  // per * 32 <= SUB: no overflow
-    const int fb = c * 32;
-    const int r = fb / n, j = fb - r * n + lane;
-    const int32_t *row = cand + ((int64_t)r * T + t) * words;
-    const uint32_t w = static_cast<uint32_t>(__ldg(row + j));
-    const uint32_t plane = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
-    const uint32_t key = bprime_list_key(w);
-    const unsigned b = __ballot_sync(kFull, key != 0u);
-    if (key != 0u) {
-      const int pos = cnt + __popc(b & lt);
-      if (satk_check(pos < SUB, kDbgList)) {
-        lk[pos] = key;
-        lv[pos] = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
+  // per * 32 <= SUB: no overflow.  The words of up to kLoadBatch chunks
+  // are loaded before any is listed, so their latencies overlap.
+  constexpr int kLoadBatch = 8;
+  for (int cb = c0; cb < c1; cb += kLoadBatch) {
+    uint32_t wv[kLoadBatch], pv[kLoadBatch];
+    int rv[kLoadBatch], jv[kLoadBatch];
+#pragma unroll
+    for (int q = 0; q < kLoadBatch; ++q) {
+      const int c = cb + q;
+      wv[q] = 0u;
+      pv[q] = 0u;
+      rv[q] = 0;
+      jv[q] = 0;
+      if (c < c1) {
+        const int fb = c * 32;
+        const int r = fb / n, j = fb - r * n + lane;
+        const int32_t *row = cand + ((int64_t)r * T + t) * words;
+        wv[q] = static_cast<uint32_t>(__ldg(row + j));
+        pv[q] = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
+        rv[q] = r;
+        jv[q] = j;
       }
-      kmn = min(kmn, key);
-      kmx = max(kmx, key);
     }
-    cnt += __popc(b);
+#pragma unroll
+    for (int q = 0; q < kLoadBatch; ++q) {
+      if (cb + q < c1) {  // warp-uniform
+        const uint32_t key = bprime_list_key(wv[q]);
+        const unsigned b = __ballot_sync(kFull, key != 0u);
+        if (key != 0u) {
+          const int pos = cnt + __popc(b & lt);
+          if (satk_check(pos < SUB, kDbgList)) {
+            lk[pos] = key;
+            lv[pos] = bprime_local(wv[q], pv[q], jv[q]) * (uint32_t)W + (uint32_t)rv[q];
+          }
+          kmn = min(kmn, key);
+          kmx = max(kmx, key);
+        }
+        cnt += __popc(b);
+      }
+    }
   }
   const WarpStats st{cnt, __reduce_min_sync(kFull, kmn), __reduce_max_sync(kFull, kmx)};
   __syncthreads();

@@ -259,43 +259,65 @@ __global__ void __launch_bounds__(BLOCK) rescue_select_kernel(
   uint32_t *lv = sm.val + warp * SUB;
   int cnt = 0;
   uint32_t kmn = 0xffffffffu, kmx = 0u;
-  for (int c = c0; c < c1; ++c) {
-    const int fb = c * 32;
-    uint32_t key = 0u, gid = 0u;
-    if (fb < r1) {
-      const int r = fb / n, j = fb - r * n + lane;
-      if (((mask >> r) & 1u) == 0u) {
-        const int32_t *row = packed + ((int64_t)r * T + t) * words_r1;
-        const uint32_t w = static_cast<uint32_t>(__ldg(row + j));
-        const uint32_t plane = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
-        key = bprime_list_key(w);
-        gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)r;
+  // the words of up to kLoadBatch chunks are loaded before any is listed,
+  // so their latencies overlap
+  constexpr int kLoadBatch = 8;
+  bool over = false;
+  for (int cb = c0; cb < c1 && !over; cb += kLoadBatch) {
+    uint32_t wv[kLoadBatch], pv[kLoadBatch], ov[kLoadBatch];
+    int jv[kLoadBatch];
+#pragma unroll
+    for (int q = 0; q < kLoadBatch; ++q) {
+      const int c = cb + q;
+      wv[q] = 0u;
+      pv[q] = 0u;
+      ov[q] = 0u;
+      jv[q] = 0;
+      if (c < c1) {
+        const int fb = c * 32;
+        if (fb < r1) {
+          const int r = fb / n, j = fb - r * n + lane;
+          if (((mask >> r) & 1u) == 0u) {
+            const int32_t *row = packed + ((int64_t)r * T + t) * words_r1;
+            wv[q] = static_cast<uint32_t>(__ldg(row + j));
+            pv[q] = static_cast<uint32_t>(__ldg(row + n + ((j - lane) >> 5)));
+          }
+          ov[q] = static_cast<uint32_t>(r);
+          jv[q] = j;
+        } else {
+          const int qq = fb - r1;
+          const int s = qq / K, j = qq - s * K + lane;
+          const int32_t *sl = recv + ((int64_t)t * slots + s) * words_k;
+          wv[q] = static_cast<uint32_t>(sl[j]);
+          pv[q] = static_cast<uint32_t>(sl[K + ((j - lane) >> 5)]);
+          ov[q] = static_cast<uint32_t>(nth_set_bit(mask, s));
+          jv[q] = j;
+        }
       }
-    } else {
-      const int q = fb - r1;
-      const int s = q / K, j = q - s * K + lane;
-      const int32_t *sl = recv + ((int64_t)t * slots + s) * words_k;
-      const uint32_t w = static_cast<uint32_t>(sl[j]);
-      const uint32_t plane = static_cast<uint32_t>(sl[K + ((j - lane) >> 5)]);
-      key = bprime_list_key(w);
-      gid = bprime_local(w, plane, j) * (uint32_t)W + (uint32_t)nth_set_bit(mask, s);
     }
-    if (key <= tau) key = 0u;  // ord16 below the round-1 cut (or empty); keys are ord16 + 1
-    const unsigned b = __ballot_sync(kFull, key != 0u);
-    if (cnt + __popc(b) > SUB) {  // warp-uniform
-      if (lane == 0) sm.flag = 1;
-      break;
-    }
-    if (key != 0u) {
-      const int pos = cnt + __popc(b & lt);
-      if (satk_check(pos < SUB, kDbgList)) {
-        lk[pos] = key;
-        lv[pos] = gid;
+#pragma unroll
+    for (int q = 0; q < kLoadBatch; ++q) {
+      if (cb + q < c1 && !over) {  // warp-uniform
+        uint32_t key = bprime_list_key(wv[q]);
+        if (key <= tau) key = 0u;  // ord16 below the round-1 cut (or empty); keys are ord16 + 1
+        const unsigned b = __ballot_sync(kFull, key != 0u);
+        if (cnt + __popc(b) > SUB) {  // warp-uniform
+          if (lane == 0) sm.flag = 1;
+          over = true;
+        } else {
+          if (key != 0u) {
+            const int pos = cnt + __popc(b & lt);
+            if (satk_check(pos < SUB, kDbgList)) {
+              lk[pos] = key;
+              lv[pos] = bprime_local(wv[q], pv[q], jv[q]) * (uint32_t)W + ov[q];
+            }
+            kmn = min(kmn, key);
+            kmx = max(kmx, key);
+          }
+          cnt += __popc(b);
+        }
       }
-      kmn = min(kmn, key);
-      kmx = max(kmx, key);
     }
-    cnt += __popc(b);
   }
   const WarpStats st{cnt, __reduce_min_sync(kFull, kmn), __reduce_max_sync(kFull, kmx)};
   __syncthreads();
