@@ -68,6 +68,35 @@ __device__ __forceinline__ uint32_t load_raw(const T *p) {
 
 // ------------------------------------------------------------ threshold --
 
+// A float as an int with the same order (for warp and block minima and maxima).
+__device__ __forceinline__ int float_order(float f) {
+  const int i = __float_as_int(f);
+  return i ^ ((i >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float float_of_order(int i) {
+  return __int_as_float(i ^ ((i >> 31) & 0x7fffffff));
+}
+
+// Bin of x in a value-linear histogram of 256 bins starting at lo, sc bins
+// per unit; values below lo go to bin 0, above the top to bin 255.
+__device__ __forceinline__ int value_bin(float x, float lo, float sc) {
+  return min(255, max(0, __float2int_rz((x - lo) * sc)));
+}
+
+// The largest value of T's grid at or below t (bf16 thresholds compare
+// exactly as floats only on the bf16 grid).
+template <typename T>
+__device__ __forceinline__ float grid_floor(float t) {
+  if constexpr (std::is_same<T, float>::value) {
+    return t;
+  } else {
+    uint32_t b = __float_as_uint(t);
+    b = (b & 0x80000000u) ? ((b + 0xffffu) & 0xffff0000u) : (b & 0xffff0000u);
+    return __uint_as_float(b);
+  }
+}
+
+
 // Loads the sample of a row: BLOCK*SPT columns in BLOCK*SPT/32 runs of 32
 // consecutive columns spread evenly over [0, end), one coalesced load per
 // warp and run, so the sample touches few memory sectors.  Their keys go to
@@ -112,6 +141,76 @@ __device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
   const int r = sample_rank(K, BLOCK * SPT, end);
   const Sel s = list_select<BLOCK>([&](int i) { return sm.key[i]; }, sg, r, sm.sel, 3);
   return s.take_all ? 1u : s.T;
+}
+
+// T0 of a row from a value-linear histogram of the same sample (the values,
+// kept in registers): 256 bins over the sample's [min, max], the r-th
+// largest value's bin edge (one finer pass inside a bin holding more than
+// 32 samples).  One pass and three block barriers where the ordered-key
+// digits take up to three passes; ok = false when the range is not usable
+// (an infinity, a single value) and the caller takes sample_threshold.
+// -inf: every valid column.  On T's grid.
+template <typename T, int BLOCK, int SPT, int SUB>
+__device__ float value_sample_threshold(const T *__restrict__ xr, int end, int K,
+                                        ListSmem<BLOCK, SUB> &sm, bool &ok) {
+  constexpr int NRUNS = BLOCK * SPT / 32;
+  constexpr int NW = BLOCK / 32;
+  const int lane = lane_id(), warp = warp_id();
+  float v[SPT];
+  float mn = __uint_as_float(0x7f800000u), mx = __uint_as_float(0xff800000u);
+#pragma unroll
+  for (int q = 0; q < SPT; ++q) {
+    const int run = warp * SPT + q;
+    const int start = static_cast<int>((static_cast<int64_t>(run) * end) / NRUNS) & ~31;
+    v[q] = as_float<T>(load_raw(xr + start + lane));
+    mn = fminf(mn, v[q]);  // NaN ignored
+    mx = fmaxf(mx, v[q]);
+  }
+  const int wmn = __reduce_min_sync(kFull, float_order(mn));
+  const int wmx = __reduce_max_sync(kFull, float_order(mx));
+  if (lane == 0) {
+    sm.sel.wtot[1][warp] = wmn;
+    sm.sel.wtot[2][warp] = wmx;
+  }
+  __syncthreads();
+  int imn = sm.sel.wtot[1][0], imx = sm.sel.wtot[2][0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) {
+    imn = min(imn, sm.sel.wtot[1][w]);
+    imx = max(imx, sm.sel.wtot[2][w]);
+  }
+  mn = float_of_order(imn);
+  mx = float_of_order(imx);
+  ok = true;
+  const float ninf = __uint_as_float(0xff800000u);
+  if (mx < mn) return ninf;  // no valid sample (block-uniform)
+  const float span = mx - mn;
+  if (!(span > 0.f) || !(span < __uint_as_float(0x7f800000u))) {
+    ok = false;
+    return 0.f;
+  }
+  const int r = sample_rank(K, BLOCK * SPT, end);
+  const float sc = 256.f * __frcp_rn(span);
+#pragma unroll
+  for (int q = 0; q < SPT; ++q)
+    if (v[q] == v[q]) atomicAdd(sm.sel.hist + value_bin(v[q], mn, sc), 1u);
+  __syncthreads();
+  const PassOut p = find_threshold<BLOCK, 256>(sm.sel, r);
+  if (p.d < 0) return ninf;  // fewer than r valid samples
+  float t = mn + static_cast<float>(p.d) * __frcp_rn(sc);
+  if (p.cnt > 32 && p.d < 255) {  // block-uniform: a crowded bin, a finer pass inside it
+    const float sc2 = sc * 256.f;
+    const float lo2 = t;
+#pragma unroll
+    for (int q = 0; q < SPT; ++q)
+      if (v[q] == v[q] && value_bin(v[q], mn, sc) == p.d)
+        atomicAdd(sm.sel.hist + value_bin(v[q], lo2, sc2), 1u);
+    __syncthreads();
+    const PassOut p2 = find_threshold<BLOCK, 256>(sm.sel, r - p.above);
+    t = lo2 + static_cast<float>(p2.d) * __frcp_rn(sc2);
+  }
+  // a little below the bin's edge, so rounding drops no counted sample
+  return grid_floor<T>(t - fabsf(t) * 9.5367e-7f - 1e-37f);
 }
 
 // ---------------------------------------------------- single-pass filter --
@@ -574,7 +673,10 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   if (all) {
     t0f = __uint_as_float(0xff800000u);  // -inf: every valid column
   } else {
-    t0f = threshold_float<KB>(sample_threshold<T, BLOCK, kRowSample, SUB>(xr, end, K, sm));
+    bool ok;
+    t0f = value_sample_threshold<T, BLOCK, kRowSample, SUB>(xr, end, K, sm, ok);
+    if (!ok)  // block-uniform
+      t0f = threshold_float<KB>(sample_threshold<T, BLOCK, kRowSample, SUB>(xr, end, K, sm));
   }
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear

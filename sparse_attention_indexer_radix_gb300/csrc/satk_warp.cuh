@@ -53,34 +53,6 @@ struct WarpRange {
   uint32_t mn, mx;
 };
 
-// Warp minimum / maximum of a float through an int map with the same order.
-__device__ __forceinline__ int float_order(float f) {
-  const int i = __float_as_int(f);
-  return i ^ ((i >> 31) & 0x7fffffff);
-}
-__device__ __forceinline__ float float_of_order(int i) {
-  return __int_as_float(i ^ ((i >> 31) & 0x7fffffff));
-}
-
-// Bin of x in a value-linear histogram of 256 bins starting at lo, sc bins
-// per unit; values below lo go to bin 0, above the top to bin 255.
-__device__ __forceinline__ int value_bin(float x, float lo, float sc) {
-  return min(255, max(0, __float2int_rz((x - lo) * sc)));
-}
-
-// The largest value of T's grid at or below t (bf16 thresholds compare
-// exactly as floats only on the bf16 grid).
-template <typename T>
-__device__ __forceinline__ float grid_floor(float t) {
-  if constexpr (std::is_same<T, float>::value) {
-    return t;
-  } else {
-    uint32_t b = __float_as_uint(t);
-    b = (b & 0x80000000u) ? ((b + 0xffffu) & 0xffff0000u) : (b & 0xffff0000u);
-    return __uint_as_float(b);
-  }
-}
-
 // Sampled columns of a row of end > kWarpList columns: runs of 32 8-column
 // groups, one vector load per lane and run, spread evenly over the row, as
 // many runs (at most kWarpSample / 256) as keep the expected list plus four
