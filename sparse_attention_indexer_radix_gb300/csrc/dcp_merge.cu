@@ -14,8 +14,8 @@
 #include <climits>
 
 #include "satk_host.hpp"
-#include "satk_list.cuh"
 #include "satk_merge.cuh"
+#include "satk_rows.cuh"
 
 namespace satk {
 namespace {
@@ -233,19 +233,26 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   if (!all) {
     constexpr int S = BLOCK * SPT;
     constexpr int NRUNS = S / 32;  // runs of 32 consecutive candidates
+    float v[SPT];  // sampled scores, NaN for an empty pair
 #pragma unroll
     for (int q = 0; q < SPT; ++q) {
       const int run = warp * SPT + q;
       const int f = (static_cast<int>((static_cast<int64_t>(run) * total) / NRUNS) & ~31) + lane;
-      sm.key[warp * SUB + q * 32 + lane] = pair_key(__ldg(at(f)));
+      const int2 pr = __ldg(at(f));
+      v[q] = pr.y >= 0 ? __int_as_float(pr.x) : __uint_as_float(0x7fc00000u);
     }
-    const float mu = static_cast<float>(K) * S / static_cast<float>(total);
-    int r = static_cast<int>(ceilf(mu + 4.f * sqrtf(mu) + 4.f));
-    r = r < 1 ? 1 : (r > S ? S : r);
-    __syncwarp();
-    const Sel sl = list_select<BLOCK>([&](int i) { return sm.key[i]; },
-                                      Seg{warp * SUB, 32 * SPT}, r, sm.sel, 3);
-    t0f = threshold_float<32>(sl.take_all ? 1u : sl.T);
+    const int r = sample_rank(K, S, total);
+    bool ok;
+    t0f = block_value_threshold<BLOCK, SPT>(v, r, sm.sel, ok);
+    if (!ok) {  // block-uniform: an unusable value range, rank by ordered keys
+#pragma unroll
+      for (int q = 0; q < SPT; ++q)
+        sm.key[warp * SUB + q * 32 + lane] = key_f32(__float_as_uint(v[q]));
+      __syncwarp();
+      const Sel sl = list_select<BLOCK>([&](int i) { return sm.key[i]; },
+                                        Seg{warp * SUB, 32 * SPT}, r, sm.sel, 3);
+      t0f = threshold_float<32>(sl.take_all ? 1u : sl.T);
+    }
     __syncthreads();
   }
 
@@ -350,34 +357,56 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
       if (above + p.cnt <= CAP || pbits == 32) break;
     }
     const uint32_t thr = take_all ? 1u : (prefix << (32 - pbits));
-    // ordered collection (flat order) of keys >= thr; at full resolution a
-    // tie wider than the list keeps the first `need` tied pairs
+    // At full resolution a tie wider than the list: the order among equal
+    // scores is the global id, so find the `need`-th smallest id among the
+    // tied pairs (digits of ~id from the top, 11/11/10 bits) and keep the
+    // tied pairs with an id at or below it.
     const bool limited = !take_all && pbits == 32;
-    int runA = 0, runB = 0, par = 0;
+    uint32_t gmax = 0u;  // with limited: the largest id kept among the ties
+    if (limited) {
+      uint32_t gp = 0u;
+      int gbits = 0, gneed = need;
+      while (gbits < 32) {
+        const int width = min(11, 32 - gbits);
+        const int shift = 32 - gbits - width;
+        for (int f = threadIdx.x; f < total; f += BLOCK) {
+          const int2 pr = __ldg(at(f));
+          if (pair_key(pr) == thr) {
+            const uint32_t u = 0xffffffffu - static_cast<uint32_t>(pr.y);
+            if (gbits == 0 || (u >> (32 - gbits)) == gp)
+              atomicAdd(sm.sel.hist + ((u >> shift) & ((1u << width) - 1u)), 1u);
+          }
+        }
+        __syncthreads();
+        const PassOut p = find_threshold<BLOCK, 2048>(sm.sel, gneed);
+        if (p.d < 0) break;  // not reached: at least `need` pairs tie at thr
+        gneed -= p.above;
+        gp = (gp << width) | static_cast<uint32_t>(p.d);
+        gbits += width;
+      }
+      gmax = 0xffffffffu - gp;
+    }
+    // collection (flat order) of the chosen pairs' keys and ids
+    int run = 0, par = 0;
     for (int f0 = 0; f0 < total; f0 += BLOCK) {
       const int f = f0 + threadIdx.x;
-      const uint32_t k = f < total ? pair_key(__ldg(at(f))) : 0u;
-      const bool a = limited ? k > thr : k >= thr;
-      const bool b = limited && k == thr;
-      const unsigned ba = __ballot_sync(kFull, a), bb = __ballot_sync(kFull, b);
+      const int2 pr = f < total ? __ldg(at(f)) : make_int2(0, -1);
+      const uint32_t k = pair_key(pr);
+      const bool keep = limited ? (k > thr || (k == thr && static_cast<uint32_t>(pr.y) <= gmax))
+                                : (k != 0u && k >= thr);
+      const unsigned bk = __ballot_sync(kFull, keep);
       int tot2;
-      const unsigned wb = (unsigned)block_warp_prefix<BLOCK>((__popc(ba) << 16) | __popc(bb),
-                                                            sm.sel.wtot[par], &tot2);
+      const int wb = block_warp_prefix<BLOCK>(__popc(bk), sm.sel.wtot[par], &tot2);
       par ^= 1;
-      const int pa = runA + (int)(wb >> 16) + __popc(ba & ((1u << lane) - 1u));
-      const int pb = runB + (int)(wb & 0xffffu) + __popc(bb & ((1u << lane) - 1u));
-      int pos = -1;
-      if (a) pos = pa + (limited ? min(pb, need) : 0);
-      if (b && pb < need) pos = pa + pb;
-      if (pos >= 0 && pos < CAP) {
+      const int pos = run + wb + __popc(bk & ((1u << lane) - 1u));
+      if (keep && satk_check(pos < CAP, kDbgList)) {
         sm.key[pos] = k;
-        sm.val[pos] = static_cast<uint32_t>(__ldg(at(f)).y);
+        sm.val[pos] = static_cast<uint32_t>(pr.y);
       }
-      runA += (int)((unsigned)tot2 >> 16);
-      runB += (int)((unsigned)tot2 & 0xffffu);
+      run += tot2;
     }
     __syncthreads();
-    const int nlist = min(CAP, runA + (limited ? min(runB, need) : 0));
+    const int nlist = min(CAP, run);
     const int chunk = (nlist + NW - 1) / NW;
     const int b0 = min(nlist, warp * chunk);
     sg = Seg{b0, min(nlist, b0 + chunk) - b0};

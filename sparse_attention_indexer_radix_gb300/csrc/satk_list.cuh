@@ -123,6 +123,12 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
     r.need = 0;
     return r;
   }
+  if (b == 0 && total == K) {  // exactly K keys, all equal: no tie to break
+    r.T = mn;
+    r.need = K;
+    r.exact = true;
+    return r;
+  }
   int need = K;
   uint32_t prefix = 0u;
   int pbits = 0;

@@ -143,41 +143,37 @@ __device__ uint32_t sample_threshold(const T *__restrict__ xr, int end, int K,
   return s.take_all ? 1u : s.T;
 }
 
-// T0 of a row from a value-linear histogram of the same sample (the values,
-// kept in registers): 256 bins over the sample's [min, max], the r-th
-// largest value's bin edge (one finer pass inside a bin holding more than
-// 32 samples).  One pass and three block barriers where the ordered-key
-// digits take up to three passes; ok = false when the range is not usable
-// (an infinity, a single value) and the caller takes sample_threshold.
-// -inf: every valid column.  On T's grid.
-template <typename T, int BLOCK, int SPT, int SUB>
-__device__ float value_sample_threshold(const T *__restrict__ xr, int end, int K,
-                                        ListSmem<BLOCK, SUB> &sm, bool &ok) {
-  constexpr int NRUNS = BLOCK * SPT / 32;
+// The threshold of a block's sample of SPT values per thread (NaN: no
+// candidate) for rank r: a value-linear histogram of 256 bins over the
+// sample's [min, max], the r-th largest value's bin edge (one finer pass
+// inside a bin holding more than 32 samples), a little below the edge so
+// that rounding drops no counted sample.  One pass and three block
+// barriers where the ordered-key digits take up to three passes.  -inf when
+// fewer than r values are valid; ok = false when the range is not usable
+// (an infinity, a single value): the caller then ranks by ordered keys.
+template <int BLOCK, int SPT>
+__device__ float block_value_threshold(const float (&v)[SPT], int r, SelectSmem<BLOCK> &sel,
+                                       bool &ok) {
   constexpr int NW = BLOCK / 32;
   const int lane = lane_id(), warp = warp_id();
-  float v[SPT];
   float mn = __uint_as_float(0x7f800000u), mx = __uint_as_float(0xff800000u);
 #pragma unroll
   for (int q = 0; q < SPT; ++q) {
-    const int run = warp * SPT + q;
-    const int start = static_cast<int>((static_cast<int64_t>(run) * end) / NRUNS) & ~31;
-    v[q] = as_float<T>(load_raw(xr + start + lane));
     mn = fminf(mn, v[q]);  // NaN ignored
     mx = fmaxf(mx, v[q]);
   }
   const int wmn = __reduce_min_sync(kFull, float_order(mn));
   const int wmx = __reduce_max_sync(kFull, float_order(mx));
   if (lane == 0) {
-    sm.sel.wtot[1][warp] = wmn;
-    sm.sel.wtot[2][warp] = wmx;
+    sel.wtot[1][warp] = wmn;
+    sel.wtot[2][warp] = wmx;
   }
   __syncthreads();
-  int imn = sm.sel.wtot[1][0], imx = sm.sel.wtot[2][0];
+  int imn = sel.wtot[1][0], imx = sel.wtot[2][0];
 #pragma unroll
   for (int w = 1; w < NW; ++w) {
-    imn = min(imn, sm.sel.wtot[1][w]);
-    imx = max(imx, sm.sel.wtot[2][w]);
+    imn = min(imn, sel.wtot[1][w]);
+    imx = max(imx, sel.wtot[2][w]);
   }
   mn = float_of_order(imn);
   mx = float_of_order(imx);
@@ -186,16 +182,18 @@ __device__ float value_sample_threshold(const T *__restrict__ xr, int end, int K
   if (mx < mn) return ninf;  // no valid sample (block-uniform)
   const float span = mx - mn;
   if (!(span > 0.f) || !(span < __uint_as_float(0x7f800000u))) {
+    // block-uniform; the caller's fallback select writes wtot[1] and
+    // wtot[2] next, so every warp must have read them first
+    __syncthreads();
     ok = false;
     return 0.f;
   }
-  const int r = sample_rank(K, BLOCK * SPT, end);
   const float sc = 256.f * __frcp_rn(span);
 #pragma unroll
   for (int q = 0; q < SPT; ++q)
-    if (v[q] == v[q]) atomicAdd(sm.sel.hist + value_bin(v[q], mn, sc), 1u);
+    if (v[q] == v[q]) atomicAdd(sel.hist + value_bin(v[q], mn, sc), 1u);
   __syncthreads();
-  const PassOut p = find_threshold<BLOCK, 256>(sm.sel, r);
+  const PassOut p = find_threshold<BLOCK, 256>(sel, r);
   if (p.d < 0) return ninf;  // fewer than r valid samples
   float t = mn + static_cast<float>(p.d) * __frcp_rn(sc);
   if (p.cnt > 32 && p.d < 255) {  // block-uniform: a crowded bin, a finer pass inside it
@@ -204,13 +202,31 @@ __device__ float value_sample_threshold(const T *__restrict__ xr, int end, int K
 #pragma unroll
     for (int q = 0; q < SPT; ++q)
       if (v[q] == v[q] && value_bin(v[q], mn, sc) == p.d)
-        atomicAdd(sm.sel.hist + value_bin(v[q], lo2, sc2), 1u);
+        atomicAdd(sel.hist + value_bin(v[q], lo2, sc2), 1u);
     __syncthreads();
-    const PassOut p2 = find_threshold<BLOCK, 256>(sm.sel, r - p.above);
+    const PassOut p2 = find_threshold<BLOCK, 256>(sel, r - p.above);
     t = lo2 + static_cast<float>(p2.d) * __frcp_rn(sc2);
   }
-  // a little below the bin's edge, so rounding drops no counted sample
-  return grid_floor<T>(t - fabsf(t) * 9.5367e-7f - 1e-37f);
+  return t - fabsf(t) * 9.5367e-7f - 1e-37f;
+}
+
+// T0 of a row from block_value_threshold over the same sample as
+// sample_threshold (the values kept in registers).  On T's grid.
+template <typename T, int BLOCK, int SPT, int SUB>
+__device__ float value_sample_threshold(const T *__restrict__ xr, int end, int K,
+                                        ListSmem<BLOCK, SUB> &sm, bool &ok) {
+  constexpr int NRUNS = BLOCK * SPT / 32;
+  const int lane = lane_id(), warp = warp_id();
+  float v[SPT];
+#pragma unroll
+  for (int q = 0; q < SPT; ++q) {
+    const int run = warp * SPT + q;
+    const int start = static_cast<int>((static_cast<int64_t>(run) * end) / NRUNS) & ~31;
+    v[q] = as_float<T>(load_raw(xr + start + lane));
+  }
+  const float t = block_value_threshold<BLOCK, SPT>(v, sample_rank(K, BLOCK * SPT, end), sm.sel,
+                                                    ok);
+  return grid_floor<T>(t);
 }
 
 // ---------------------------------------------------- single-pass filter --

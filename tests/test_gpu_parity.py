@@ -381,6 +381,69 @@ def test_pairs_merge_ties_empties_and_short_rows():
         assert_rows_equal(got, want, f"pairs ties k={kk}")
 
 
+def test_pairs_merge_sampled_threshold_edge_ranges():
+    """Rows with more candidates than the list holds take the sampled
+    value threshold; these rows give it the ranges it must not trust or
+    must refine: an infinity among the scores, a single score value, a few
+    levels (a crowded histogram bin), an overflowing span (-3e38 .. 3e38),
+    mostly empty pairs (fewer valid samples than the rank), and signed
+    zeros with NaN."""
+    W, T, n = 8, 8, 2048
+    g = torch.Generator().manual_seed(77)
+    sc = torch.randn((W, T, n), generator=g)
+    sc[:, 0, ::97] = float("inf")
+    sc[:, 1] = 1.5
+    sc[:, 2] = torch.randint(0, 4, (W, n), generator=g).float()
+    sc[:, 3, ::2] = 3e38
+    sc[:, 3, 1::2] = -3e38
+    sc[:, 5] = torch.tensor([-0.0, 0.0, float("nan"), 1e-30])[
+        torch.randint(0, 4, (W, n), generator=g)]
+    sc[:, 6, ::5] = float("-inf")
+    gid = torch.randperm(W * T * n, generator=g).view(W, T, n).to(torch.int32)
+    gid[:, 4, 7:] = -1                                    # mostly empty
+    gid[:, 7, ::2] = -1                                   # half empty
+    cand = torch.stack([sc.contiguous().view(torch.int32), gid], dim=-1).contiguous()
+    for kk in (1, 100, 2048, 3000):
+        got = satk.dcp_merge_select(cand.to(DEV), kk, packed=False).cpu().numpy()
+        want = oracle.merge_pairs(cand.numpy(), kk)
+        assert_rows_equal(got, want, f"pairs edge ranges k={kk}")
+
+
+@pytest.mark.parametrize("W,n", [(2, 32), (8, 2048)])
+def test_merges_exactly_k_equal_candidates(W, n):
+    """Rows that hold exactly K non-empty candidates, all with the same
+    score (K = 1: a single candidate): nothing is tied beyond the K-th, so
+    every candidate is chosen -- on the pairs merge (the list path below
+    the list's capacity, the sampled path above it) and on the packed list
+    engine."""
+    T = 6
+    g = torch.Generator().manual_seed(W * n)
+    for kk in (1, 3):
+        sc = torch.full((W, T, n), 0.75)
+        gid = torch.full((W, T, n), -1, dtype=torch.int32)
+        for t in range(T):
+            slots = torch.randperm(W * n, generator=g)[:kk]
+            for f in slots.tolist():
+                gid[f // n, t, f % n] = torch.randint(0, 1 << 20, (1,), generator=g).item() * W
+        cand = torch.stack([sc.contiguous().view(torch.int32), gid], dim=-1).contiguous()
+        got = satk.dcp_merge_select(cand.to(DEV), kk, packed=False).cpu().numpy()
+        want = oracle.merge_pairs(cand.numpy(), kk)
+        assert (want >= 0).all()
+        assert_rows_equal(got, want, f"pairs exactly {kk} W={W} n={n}")
+    if W * n > 4096:
+        return
+    words = n + n // 32
+    for kk in (1, 3):
+        packed = torch.zeros((W, T, words), dtype=torch.int32)
+        for t in range(T):
+            for f in torch.randperm(W * n, generator=g)[:kk].tolist():
+                packed[f // n, t, f % n] = (0x4100 << 16) | (0xffff - (f % n) * 3)
+        ids = satk.dcp_merge_select(packed.to(DEV), kk, packed=True).cpu().numpy()
+        o_ids, _, _ = oracle.merge_packed(packed.numpy(), kk)
+        assert (o_ids >= 0).all()
+        assert_rows_equal(ids, o_ids, f"packed exactly {kk}")
+
+
 def test_pairs_merge_full_size_every_row():
     """The rank-major merge workload at full size (W = 8, 6710 rows, 8 x
     2048 candidates per row, K = 2048): every row against the oracle."""
