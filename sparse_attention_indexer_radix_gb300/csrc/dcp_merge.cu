@@ -171,54 +171,74 @@ __device__ __forceinline__ uint32_t pair_key(int2 p) {
   return p.y >= 0 ? key_f32(static_cast<uint32_t>(p.x)) : 0u;
 }
 
-// 4 consecutive pairs of one lane (32 bytes): w[2s] score bits, w[2s+1] gid.
-struct Pairs4 {
-  uint32_t w[8];
-  template <int ALIGN>
-  __device__ __forceinline__ void load(const int2 *p);
-  // kept mask: bit s set when pair s is non-empty and scores >= t
-  __device__ __forceinline__ uint32_t mask(float t) const {
-    uint32_t m = 0u;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const bool keep = __uint_as_float(w[2 * s]) >= t && static_cast<int32_t>(w[2 * s + 1]) >= 0;
-      m |= (keep ? 1u : 0u) << s;
-    }
-    return m;
-  }
-};
+// One pair, streamed (read once: no L1 allocation).
+__device__ __forceinline__ int2 ldg_stream(const int2 *p) {
+  int2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.s32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
 
-template <int ALIGN>
-__device__ __forceinline__ void Pairs4::load(const int2 *p) {
-  if constexpr (ALIGN == 32) {
-    asm volatile(
-        "ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
-          "=r"(w[7])
-        : "l"(p));
-  } else {
-    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
-    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+// Brings the n pairs of each rank for row t into L2 (one bulk prefetch per
+// rank: the rank's slots of a row are contiguous, n * 8 bytes, 256-byte
+// aligned when the buffer is 16-byte aligned and n % 32 == 0).
+__device__ __forceinline__ void prefetch_row_l2(const int2 *cand, int W, int64_t T, int n,
+                                                int64_t t) {
+  for (int r = 0; r < W; ++r) {
+    const int2 *p = cand + (static_cast<int64_t>(r) * T + t) * n;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 :
+                 : "l"(p), "r"(static_cast<uint32_t>(n) * 8u)
+                 : "memory");
   }
 }
 
-template <int BLOCK, int SUB, int ALIGN>
-__global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
-    const int2 *__restrict__ cand, int W, int64_t T, int n, int K, int32_t *__restrict__ ids,
-    int64_t ld_out, int32_t *__restrict__ status) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+constexpr int kPairsSPT = 4;  // sampled pairs per thread
+
+template <int BLOCK, int SUB>
+struct PairsSmem {
+  ListSmem<BLOCK, SUB> ls;
+  int2 samp[kPairsSPT * BLOCK];  // the row's sample, [q][thread]
+};
+
+// Asynchronous copies (no registers held) of this thread's kPairsSPT
+// sampled pairs of row t into samp: the runs of 32 consecutive candidates
+// spread evenly over the flat range, lane l taking candidate l of a run.
+template <int BLOCK>
+__device__ __forceinline__ void pairs_sample_async(int2 *samp, const int2 *cand, int total,
+                                                   int64_t T, int n, int64_t t) {
+  constexpr int NRUNS = BLOCK * kPairsSPT / 32;
+#pragma unroll
+  for (int q = 0; q < kPairsSPT; ++q) {
+    const int run = warp_id() * kPairsSPT + q;
+    const int f = (static_cast<int>((static_cast<int64_t>(run) * total) / NRUNS) & ~31) + lane_id();
+    const int r = f / n;
+    const int2 *src = cand + ((static_cast<int64_t>(r) * T + t) * n + (f - r * n));
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(samp + q * BLOCK + threadIdx.x));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// One row t of the pairs merge; `next` (or -1) is the row this CTA takes
+// after it: once this row's pairs are read, the next row's pairs are
+// prefetched into L2 and its sample is copied into shared memory, so that
+// HBM keeps streaming while this row's list select runs.
+template <int BLOCK, int SUB>
+__device__ __forceinline__ void pairs_merge_row(PairsSmem<BLOCK, SUB> &ps,
+                                                const int2 *__restrict__ cand, int W, int64_t T,
+                                                int n, int K, int32_t *__restrict__ ids,
+                                                int64_t ld_out, int32_t *__restrict__ status,
+                                                const int64_t t, const int64_t next) {
   using SM = ListSmem<BLOCK, SUB>;
-  auto &sm = *reinterpret_cast<SM *>(smem_raw);
+  SM &sm = ps.ls;
   constexpr int NW = BLOCK / 32;
   constexpr int CAP = SM::CAP;
-  constexpr int SPT = 4;
-  constexpr int U = 4;
-  const int64_t t = blockIdx.x;
+  constexpr int SPT = kPairsSPT;
+  constexpr int U = 8;  // steps loaded before any is taken
   const int lane = lane_id(), warp = warp_id();
   const int total = W * n;
-  const int gpr = n / 4;  // 4-pair groups per rank
   auto at = [&](int f) {  // pair of flat candidate f
     const int r = f / n;
     return cand + ((static_cast<int64_t>(r) * T + t) * n + (f - r * n));
@@ -232,13 +252,12 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   float t0f = __uint_as_float(0xff800000u);
   if (!all) {
     constexpr int S = BLOCK * SPT;
-    constexpr int NRUNS = S / 32;  // runs of 32 consecutive candidates
     float v[SPT];  // sampled scores, NaN for an empty pair
+    // this thread's own copies (issued by pairs_sample_async before the row)
+    asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
     for (int q = 0; q < SPT; ++q) {
-      const int run = warp * SPT + q;
-      const int f = (static_cast<int>((static_cast<int64_t>(run) * total) / NRUNS) & ~31) + lane;
-      const int2 pr = __ldg(at(f));
+      const int2 pr = ps.samp[q * BLOCK + threadIdx.x];
       v[q] = pr.y >= 0 ? __int_as_float(pr.x) : __uint_as_float(0x7fc00000u);
     }
     const int r = sample_rank(K, S, total);
@@ -256,75 +275,62 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
     __syncthreads();
   }
 
-  // ---- filtered pass: keys and global ids of the kept pairs, flat order
-  const int ngroups = total / 4;
-  const int per = (ngroups + NW - 1) / NW;
-  const int g0 = min(ngroups, warp * per), g1 = min(ngroups, g0 + per);
-  uint32_t *lk = sm.key + warp * SUB;
-  uint32_t *lv = sm.val + warp * SUB;
+  // ---- filtered pass: keys and global ids of the kept pairs, flat order.
+  // Lane l takes pair 32 s + l of each step (one 8-byte load per pair, a
+  // warp's load is 256 contiguous bytes); a ballot per step gives every
+  // kept pair its list position in flat order.  Each warp walks a stretch
+  // of whole 32-pair steps; a step never crosses a rank (n % 32 == 0).
+  const int nsteps = total / 32;
+  const int per = (nsteps + NW - 1) / NW;
+  const int s0 = min(nsteps, warp * per), s1 = min(nsteps, s0 + per);
+  // shared addresses of this warp's key segment; a value sits CAP words
+  // after its key
+  const uint32_t lk = static_cast<uint32_t>(__cvta_generic_to_shared(sm.key + warp * SUB));
+  static_assert(offsetof(SM, val) - offsetof(SM, key) == CAP * sizeof(uint32_t),
+                "values follow the keys");
+  const unsigned lt = (1u << lane) - 1u;
   int cnt = 0;
-  uint32_t kmn = 0xffffffffu, kmx = 0u;  // range of the keys written
-  for (int gr = g0; gr < g1;) {  // runs inside one rank (warp-uniform)
-    const int r = gr / gpr;
-    const int rend = min(g1, (r + 1) * gpr);
-    const int2 *base = cand + (static_cast<int64_t>(r) * T + t) * n - static_cast<int64_t>(r) * n;
-    for (int gb = gr; gb < rend; gb += 32 * U) {
-      Pairs4 grp[U];
+  bool room = true;  // warp-uniform: no step has passed SUB entries
+  auto take = [&](const int2 v) {  // one step: 32 pairs, one per lane
+    const bool keep = __int_as_float(v.x) >= t0f && v.y >= 0;
+    const unsigned b = __ballot_sync(kFull, keep);
+    const int nc = cnt + __popc(b);
+    room = room && nc <= SUB;  // past SUB: counted only, the row takes the exact path
+    const uint32_t a = lk + 4u * static_cast<uint32_t>(cnt + __popc(b & lt));
+    // branch-free: the key and id stores are predicated on keep && room
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %0, 0;\n\t"
+        "@p st.shared.b32 [%1], %2;\n\t"
+        "@p st.shared.b32 [%1+%4], %3;\n\t}"
+        :
+        : "r"(static_cast<int>(keep && room)), "r"(a),
+          "r"(key_f32_num(static_cast<uint32_t>(v.x))), "r"(v.y), "n"(CAP * 4)
+        : "memory");
+    cnt = nc;
+  };
+  for (int sr = s0; sr < s1;) {  // runs inside one rank (warp-uniform)
+    const int f = sr * 32;
+    const int r = f / n;
+    const int send = min(s1, (r + 1) * (n / 32));
+    const int2 *p = cand + ((static_cast<int64_t>(r) * T + t) * n + (f - r * n)) + lane;
+    int sb = sr;
+    for (; sb + U <= send; sb += U, p += 32 * U) {
+      int2 v[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int gi = gb + u * 32 + lane;
-        if (gi < rend) grp[u].template load<ALIGN>(base + static_cast<int64_t>(gi) * 4);
-      }
-      uint32_t m[U];
-      uint32_t any = 0u;
+      for (int u = 0; u < U; ++u) v[u] = ldg_stream(p + 32 * u);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int gi = gb + u * 32 + lane;
-        m[u] = gi < rend ? grp[u].mask(t0f) : 0u;
-        any |= m[u];
-      }
-      if (!__any_sync(kFull, any != 0u)) continue;
-      uint32_t pk = 0u;
-#pragma unroll
-      for (int u = 0; u < U; ++u) pk |= static_cast<uint32_t>(__popc(m[u])) << (8 * u);
-      const uint32_t incl = static_cast<uint32_t>(warp_incl_scan(static_cast<int>(pk)));
-      const uint32_t tot = __shfl_sync(kFull, incl, 31);
-      const int btot = static_cast<int>((tot & 0xffu) + ((tot >> 8) & 0xffu) +
-                                        ((tot >> 16) & 0xffu) + (tot >> 24));
-      if (cnt + btot > SUB) {  // warp-uniform: the segment overflows
-        cnt += btot;
-        break;
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint32_t lc = static_cast<uint32_t>(__popc(m[u]));
-        // a quarter or more of the pairs pass: four fixed steps with the
-        // pair index known at compile time beat a loop over the set bits
-        const int pos0 = cnt + static_cast<int>(((incl >> (8 * u)) & 0xffu) - lc);
-        const uint32_t mm = m[u];
-        if (mm != 0u) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const int pos = pos0 + __popc(mm & ((1u << s) - 1u));
-            if ((mm >> s) & 1u) {
-              const uint32_t k = key_f32_num(grp[u].w[2 * s]);
-              if (satk_check(pos < SUB, kDbgList)) {
-                lk[pos] = k;
-                lv[pos] = grp[u].w[2 * s + 1];
-              }
-              kmn = min(kmn, k);
-              kmx = max(kmx, k);
-            }
-          }
-        }
-        cnt += static_cast<int>((tot >> (8 * u)) & 0xffu);
-      }
+      for (int u = 0; u < U; ++u) take(v[u]);
     }
-    gr = cnt > SUB ? g1 : rend;  // stop at an overflow
+    for (; sb < send; ++sb, p += 32) take(ldg_stream(p));
+    sr = send;
+  }
+  if (next >= 0) {
+    if (!all) pairs_sample_async<BLOCK>(ps.samp, cand, total, T, n, next);
+    if (threadIdx.x == 0) prefetch_row_l2(cand, W, T, n, next);
   }
   if (cnt > SUB && lane == 0) sm.flag = 1;
   Seg sg{warp * SUB, min(cnt, SUB)};
-  const WarpStats st{min(cnt, SUB), __reduce_min_sync(kFull, kmn), __reduce_max_sync(kFull, kmx)};
   int listed;  // wtot[3]: its next writer (the list emit) is behind barriers
   block_warp_prefix<BLOCK>(sg.cnt, sm.sel.wtot[3], &listed);
   const bool ok = sm.flag == 0 && (all || listed >= K);
@@ -416,19 +422,39 @@ __global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
   // ---- select: by score, then by global id among ties with the K-th
   int32_t *out = ids + t * ld_out;
   const bool dup = list_merge_emit<BLOCK, SUB>(
-      sm, sg, K, [&](int pos, int32_t v) { out[pos] = v; }, ok ? st : stats_unknown()).dup;
+      sm, sg, K, [&](int pos, int32_t v) { out[pos] = v; }).dup;
   if (dup && status != nullptr && threadIdx.x == 0) atomicOr(status, SATK_STATUS_DUPLICATE_KEYS);
 }
 
-template <int SUB, int ALIGN>
+// Persistent: CTA b takes rows b, b + gridDim.x, ... (the grid is the
+// resident CTA count, so each CTA's next row is known and prefetched).
+template <int BLOCK, int SUB>
+__global__ void __launch_bounds__(BLOCK, 1024 / BLOCK) pairs_merge_kernel(
+    const int2 *__restrict__ cand, int W, int64_t T, int n, int K, int32_t *__restrict__ ids,
+    int64_t ld_out, int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto &ps = *reinterpret_cast<PairsSmem<BLOCK, SUB> *>(smem_raw);
+  if (W * n > ListSmem<BLOCK, SUB>::CAP)  // the first row's sample
+    pairs_sample_async<BLOCK>(ps.samp, cand, W * n, T, n, blockIdx.x);
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    const int64_t next = t + gridDim.x < T ? t + gridDim.x : -1;
+    pairs_merge_row<BLOCK, SUB>(ps, cand, W, T, n, K, ids, ld_out, status, t, next);
+    __syncthreads();  // this row's list and histogram reads before the next row's writes
+  }
+}
+
+template <int SUB>
 int launch_pairs(const int32_t *cand, int W, int64_t T, int n, int K, int32_t *ids,
                  int64_t ld_out, int32_t *status, cudaStream_t st) {
   constexpr int BLOCK = 256;
-  auto kern = pairs_merge_kernel<BLOCK, SUB, ALIGN>;
-  const size_t smem = sizeof(ListSmem<BLOCK, SUB>);
+  auto kern = pairs_merge_kernel<BLOCK, SUB>;
+  const size_t smem = sizeof(PairsSmem<BLOCK, SUB>);
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
-  kern<<<dim3(static_cast<unsigned>(T)), BLOCK, smem, st>>>(reinterpret_cast<const int2 *>(cand),
-                                                            W, T, n, K, ids, ld_out, status);
+  const int64_t resident = resident_ctas(reinterpret_cast<const void *>(kern), BLOCK, smem);
+  if (resident < 1) return SATK_ECUDA;
+  const int64_t grid = T < resident ? T : resident;
+  kern<<<dim3(static_cast<unsigned>(grid)), BLOCK, smem, st>>>(
+      reinterpret_cast<const int2 *>(cand), W, T, n, K, ids, ld_out, status);
   return launch_status();
 }
 
@@ -617,10 +643,6 @@ extern "C" int satk_dcp_merge_select(const void *cand, int format, int32_t W, in
   if (format == SATK_PACKED_BF16)
     return dispatch_merge<true>(c, W, T, n, k, ids_out, ld_out, sat_word, status, st);
   // pairs: the list holds 8 warps x SUB candidates (4096 up to K = 2048)
-  const bool a32 = (reinterpret_cast<uintptr_t>(cand) & 31u) == 0;
-  if (k <= 2048)
-    return a32 ? launch_pairs<512, 32>(c, W, T, n, k, ids_out, ld_out, status, st)
-               : launch_pairs<512, 16>(c, W, T, n, k, ids_out, ld_out, status, st);
-  return a32 ? launch_pairs<1024, 32>(c, W, T, n, k, ids_out, ld_out, status, st)
-             : launch_pairs<1024, 16>(c, W, T, n, k, ids_out, ld_out, status, st);
+  if (k <= 2048) return launch_pairs<512>(c, W, T, n, k, ids_out, ld_out, status, st);
+  return launch_pairs<1024>(c, W, T, n, k, ids_out, ld_out, status, st);
 }
