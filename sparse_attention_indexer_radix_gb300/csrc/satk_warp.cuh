@@ -417,8 +417,9 @@ __device__ void warp_collect_exact(const T *__restrict__ xr, int end, int K, War
   __syncwarp();
 }
 
-// Select on the warp's key list and the ordered emit (dst.put(pos, key,
-// column) for positions [0, K), dst.fill past the last candidate): 8-bit
+// Select on the warp's key list and the ordered emit (dst.put_entry(pos,
+// list index, key, column) for positions [0, K), dst.fill past the last
+// candidate): 8-bit
 // digits relative to the list's key range; once the threshold digit holds
 // at most 32 keys they are ranked on the warp directly (each lane counts
 // the keys above and equal to its own) instead of more digit passes.
@@ -431,7 +432,7 @@ __device__ __forceinline__ void warp_emit(WarpRowSmem &ws, const WarpRange &lr, 
   const uint16_t *lc = ws.col();
   const int n = lr.n;
   if (n < K) {  // fewer than K: every entry in list order, then the fill
-    for (int i = lane; i < n; i += 32) dst.put(i, lk[i], static_cast<int>(lc[i]));
+    for (int i = lane; i < n; i += 32) dst.put_entry(i, i, lk[i], static_cast<int>(lc[i]));
     for (int q = n + lane; q < K; q += 32) dst.fill(q);
     return;
   }
@@ -513,10 +514,10 @@ __device__ __forceinline__ void warp_emit(WarpRowSmem &ws, const WarpRange &lr, 
     const uint32_t k = i < n ? lk[i] : 0u;
     const unsigned ba = __ballot_sync(kFull, k > v);
     const unsigned bb = __ballot_sync(kFull, k == v && i < n);
-    if ((ba >> lane) & 1u) dst.put(runA + __popc(ba & lt), k, static_cast<int>(lc[i]));
+    if ((ba >> lane) & 1u) dst.put_entry(runA + __popc(ba & lt), i, k, static_cast<int>(lc[i]));
     if ((bb >> lane) & 1u) {
       const int pb = runB + __popc(bb & lt);
-      if (pb < takeB) dst.put(cgt + pb, k, static_cast<int>(lc[i]));
+      if (pb < takeB) dst.put_entry(cgt + pb, i, k, static_cast<int>(lc[i]));
     }
     runA += __popc(ba);
     runB += __popc(bb);

@@ -10,7 +10,9 @@
 //  - rows of a few thousand columns: one warp per row (satk_warp.cuh);
 //  - few long rows: a cluster of 2-8 CTAs per row (satk_cluster.cuh);
 //  - otherwise one CTA of 128 or 256 threads per row (satk_rows.cuh).
-// The score-sorted variant runs the CTA path and sorts the chosen ids.
+// The score-sorted variant sorts the chosen ids: on the warp of a short row
+// (a bucket sort of the chosen set in registers and shared memory), else
+// after the CTA path (a block bitonic sort).
 #pragma once
 
 #include <climits>
@@ -39,7 +41,8 @@ __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, 
 
 // Where a row's chosen candidates go: put(pos, key, column) for output
 // position pos of the row's top-K layout, fill(pos) past the last one;
-// start(t, nt) runs once per row, on threads t of nt, before any put.
+// start(t, nt) runs once per row, on threads t of nt, before any put.  The
+// warp path calls put_entry(pos, list index, key, column).
 //  IdOut     -- the column ids, then -1 (satk_topk_rows).
 //  PackedOut -- the B' row of satk_dcp_topk_pack: word pos = the key's
 //               ord16 (bf16 keys are ord16 << 16) | (0xFFFF - column[15:0]),
@@ -55,6 +58,9 @@ struct IdOut {
   __device__ __forceinline__ void start(int, int) const {}
   __device__ __forceinline__ void put(int pos, uint32_t, int col) const {
     if (satk_check(pos >= 0 && pos < K, kDbgOut)) o[pos] = col;
+  }
+  __device__ __forceinline__ void put_entry(int pos, int, uint32_t key, int col) const {
+    put(pos, key, col);
   }
   __device__ __forceinline__ void fill(int pos) const {
     if (satk_check(pos >= 0 && pos < K, kDbgOut)) o[pos] = -1;
@@ -74,6 +80,9 @@ struct PackedOut {
       if (col >> 16) atomicOr(o + K + pos / 32, 1 << (pos & 31));
     }
     o[pos] = static_cast<int32_t>(w);
+  }
+  __device__ __forceinline__ void put_entry(int pos, int, uint32_t key, int col) const {
+    put(pos, key, col);
   }
   __device__ __forceinline__ void fill(int pos) const {
     if (satk_check(pos >= 0 && pos < K, kDbgOut)) o[pos] = 0;
@@ -284,6 +293,240 @@ __device__ void bitonic_sort_desc(uint64_t *buf) {
   }
 }
 
+// ---- score-sorted on one warp (short rows)
+//
+// The warp path's ordered emit records, for every output position, the
+// list index of the entry chosen there (a 16-bit map of P = 32 E entries,
+// 0xFFFF where no candidate).  The warp then gathers the chosen entries as
+// (key << 32 | ~column) composites into registers -- entry e * 32 + l in
+// lane l -- after which the list area is free for the sort's scratch:
+//  - bucket sort (the usual case): bucket b(key) = floor((key - kmin) *
+//    P / (span + 1)) is monotone in the key, so with buckets taken from
+//    the highest down an entry's output position is the count of entries
+//    in higher buckets plus its rank by composite (key desc, column asc)
+//    among its own bucket's entries, counted by a walk over the bucket;
+//  - a bitonic network over the registers when a bucket holds more than 32
+//    entries (heavy ties).
+
+struct SortMapOut {
+  uint16_t *m;
+  int K;
+  __device__ __forceinline__ void start(int, int) const {}
+  __device__ __forceinline__ void put_entry(int pos, int i, uint32_t, int) const {
+    if (satk_check(pos >= 0 && pos < K, kDbgOut)) m[pos] = static_cast<uint16_t>(i);
+  }
+  __device__ __forceinline__ void fill(int pos) const {
+    if (satk_check(pos >= 0 && pos < K, kDbgOut)) m[pos] = 0xffffu;
+  }
+};
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Compare-exchange of registers a (lower index) and b: with desc the
+// larger ends in a.
+__device__ __forceinline__ void cex(uint64_t &a, uint64_t &b, bool desc) {
+  const bool sw = desc ? a < b : a > b;
+  const uint64_t x = a;
+  a = sw ? b : a;
+  b = sw ? x : b;
+}
+
+// Bitonic sort, descending, of the 32 E values v (afterwards lane l holds
+// entries l E + e).  Pair (i, i + stride) of a block whose size bit is
+// clear ends with the larger value first; at size == P every block is such
+// a block.  Sizes up to E sort each lane's registers (unrolled); beyond E
+// only the loops over the registers are unrolled (a fully unrolled network
+// outgrows the instruction cache), and the direction of a pair is the
+// lane's.
+template <int E>
+__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[E]) {
+  constexpr int P = 32 * E;
+  const int lane = lane_id();
+#pragma unroll
+  for (int size = 2; size <= E; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((e & stride) == 0) cex(v[e], v[e + stride], ((lane * E + e) & size) == 0);
+    }
+  }
+#pragma unroll 1
+  for (int size = 2 * E; size <= P; size <<= 1) {
+    const bool desc = ((lane * E) & size) == 0;
+#pragma unroll 1
+    for (int stride = size >> 1; stride >= E; stride >>= 1) {  // partner lane ^ (stride / E)
+      const int m = stride / E;
+      const bool keep_max = desc == ((lane & m) == 0);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const uint64_t o = shfl_xor_u64(v[e], m);
+        v[e] = keep_max ? (o > v[e] ? o : v[e]) : (o < v[e] ? o : v[e]);
+      }
+    }
+#pragma unroll
+    for (int stride = E / 2; stride > 0; stride >>= 1) {  // partner register e + stride
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((e & stride) == 0) cex(v[e], v[e + stride], desc);
+    }
+  }
+}
+
+// The bucket sort over NB = 32 E buckets: composites c (0: no entry),
+// scratch tmp (32 E values), ranked columns to cols[0, n), hist (NB words)
+// zero on entry.  Returns n, the count of entries, or -1 (nothing written)
+// when a bucket holds more than 32 entries.
+template <int E>
+__device__ int warp_bucket_rank(const uint64_t (&c)[E], uint64_t *tmp, int32_t *cols,
+                                uint32_t *hist) {
+  constexpr int NB = 32 * E;
+  const int lane = lane_id();
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const uint32_t k = static_cast<uint32_t>(c[e] >> 32);
+    if (c[e] != 0u) {
+      kmn = min(kmn, k);
+      kmx = max(kmx, k);
+    }
+  }
+  kmn = __reduce_min_sync(kFull, kmn);
+  kmx = __reduce_max_sync(kFull, kmx);
+  if (kmx < kmn) return 0;  // no entry (warp-uniform)
+  const float scale = static_cast<float>(NB) / (static_cast<float>(kmx - kmn) + 1.0f);
+  int d[E];  // bucket, the highest keys in bucket 0
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const uint32_t rel = static_cast<uint32_t>(c[e] >> 32) - kmn;
+    const int b = min(NB - 1, static_cast<int>(__float2uint_rz(static_cast<float>(rel) * scale)));
+    d[e] = NB - 1 - b;
+    if (c[e] != 0u) atomicAdd(hist + d[e], 1u);
+  }
+  __syncwarp();
+  // exclusive prefix over the buckets: lane l owns buckets E l .. E l + E - 1
+  uint32_t h[E], run = 0u, big = 0u;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    h[j] = hist[E * lane + j];
+    run += h[j];
+    big = max(big, h[j]);
+  }
+  big = __reduce_max_sync(kFull, big);
+  const uint32_t n = __reduce_add_sync(kFull, run);
+  uint32_t base = static_cast<uint32_t>(warp_incl_scan(static_cast<int>(run))) - run;
+  __syncwarp();
+  if (big > 32u) return -1;  // warp-uniform
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    hist[E * lane + j] = base;
+    base += h[j];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (c[e] != 0u) tmp[atomicAdd(hist + d[e], 1u)] = c[e];
+  __syncwarp();  // hist[b] is now the end of bucket b
+  // per entry: bucket start (bits 0-9), bucket length (10-15), rank (16-)
+  uint32_t info[E];
+  uint32_t maxlen = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const uint32_t lo = d[e] == 0 ? 0u : hist[d[e] - 1];
+    const uint32_t len = c[e] != 0u ? hist[d[e]] - lo : 0u;
+    info[e] = lo | (len << 10);
+    maxlen = max(maxlen, len);
+  }
+  maxlen = __reduce_max_sync(kFull, maxlen);
+  // member j of every entry's bucket in one step: E independent loads
+  for (uint32_t j = 0; j < maxlen; ++j) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const uint32_t lo = info[e] & 1023u, len = (info[e] >> 10) & 63u;
+      if (j < len && tmp[lo + j] > c[e]) info[e] += 1u << 16;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (c[e] != 0u)
+      cols[(info[e] & 1023u) + (info[e] >> 16)] =
+          static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(c[e]));
+  __syncwarp();
+  return static_cast<int>(n);
+}
+
+// Six CTAs per SM: the sort's per-warp words push seven past the shared
+// memory.
+template <typename T, int ALIGN, int E>
+__global__ void __launch_bounds__(32 * kWarpRowsPerCta, 6)
+    topk_rows_warp_sorted_kernel(const T *__restrict__ x, int64_t rows, int64_t ld, int cols,
+                                 const int32_t *__restrict__ row_ends, int K,
+                                 int32_t *__restrict__ out, int64_t ld_out) {
+  static_assert(sizeof(uint64_t) * 32 * E + sizeof(int32_t) * 32 * E <=
+                    sizeof(WarpRowSmem::buf),
+                "the sort scratch must fit the list area");
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int warp = warp_id(), lane = lane_id();
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpRowsPerCta + warp;
+  if (row >= rows) return;  // warp-uniform; the warps never synchronise
+  WarpRowSmem &ws = reinterpret_cast<WarpRowSmem *>(smem_raw)[warp];
+  // per warp 32 E words: the index map (16-bit) during the row, the bucket
+  // counters after it
+  uint32_t *aux = reinterpret_cast<uint32_t *>(smem_raw + sizeof(WarpRowSmem) * kWarpRowsPerCta) +
+                  warp * 32 * E;
+  uint16_t *map = reinterpret_cast<uint16_t *>(aux);
+  for (int i = lane; i < 256; i += 32) ws.hist[i] = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) map[e * 32 + lane] = 0xffffu;  // positions past K: none
+  __syncwarp();
+  warp_topk_row<T, ALIGN>(x + row * ld, row_end_of(row_ends, row, cols), K, SortMapOut{map, K},
+                          ws);
+  __syncwarp();
+  uint64_t c[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const uint32_t i = map[e * 32 + lane];
+    c[e] = i == 0xffffu ? 0u
+                        : (static_cast<uint64_t>(ws.key()[i]) << 32) |
+                              (0xffffffffu - static_cast<uint32_t>(ws.col()[i]));
+  }
+  __syncwarp();  // the list and the map are read: their areas are the sort's scratch now
+#pragma unroll
+  for (int e = 0; e < E; ++e) aux[e * 32 + lane] = 0u;
+  __syncwarp();
+  uint64_t *tmp = reinterpret_cast<uint64_t *>(ws.buf);
+  int32_t *ranked = reinterpret_cast<int32_t *>(tmp + 32 * E);
+  int32_t *o = out + row * ld_out;
+  const int nb = warp_bucket_rank<E>(c, tmp, ranked, aux);
+  if (nb >= 0) {  // warp-uniform
+    for (int q = lane; q < K; q += 32) o[q] = q < nb ? ranked[q] : -1;
+    return;
+  }
+  warp_bitonic_desc<E>(c);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int q = lane * E + e;
+    if (q < K)
+      o[q] = c[e] == 0u ? -1 : static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(c[e]));
+  }
+}
+
+template <typename T, int ALIGN, int E>
+int launch_warp_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
+                       int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  auto kern = topk_rows_warp_sorted_kernel<T, ALIGN, E>;
+  const size_t smem = (sizeof(WarpRowSmem) + sizeof(uint32_t) * 32 * E) * kWarpRowsPerCta;
+  if (!allow_smem(kern, smem)) return SATK_ECUDA;
+  const int64_t grid = (rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta;
+  kern<<<dim3(static_cast<unsigned>(grid)), 32 * kWarpRowsPerCta, smem, st>>>(
+      x, rows, ld, cols, row_ends, K, out, ld_out);
+  return launch_status();
+}
+
 // The chosen set of topk_rows_kernel in score order: the row path emits
 // (key << 32 | ~column) composites into shared memory, a bitonic sort puts
 // them in descending order (key desc, then column asc), and the columns are
@@ -329,6 +572,11 @@ int launch_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t 
 template <typename T, int ALIGN>
 int launch_rows_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
                        int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
+  if (warp_rows_fit(cols, K)) {  // K <= 512: one warp per row, sort widths 128 and 512
+    if (K <= 128)
+      return launch_warp_sorted<T, ALIGN, 4>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+    return launch_warp_sorted<T, ALIGN, 16>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
+  }
   if (K <= 512)
     return launch_sorted<T, 512, ALIGN, 512>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
   if (K <= 1024)

@@ -65,6 +65,10 @@ def test_debug_build_row_paths(dbg):
         _topk_case(x, 384, None, "clustered rows")
         x, ends = inputs.prefill(rows=12, cols=9000, seed=6)
         _topk_case(x, 1000, ends, "score-sorted", sorted=True)
+        x, ends = inputs.prefill(rows=40, cols=4096, seed=8)
+        x[3] = torch.randint(0, 3, (4096,)).float()          # ties in the sort
+        _topk_case(x, 512, ends, "score-sorted warp rows", sorted=True)
+        _topk_case(x.to(torch.bfloat16), 100, ends, "score-sorted warp rows bf16", sorted=True)
         x, ends, _ = inputs.adversarial(rows=24, cols=20000, seed=7)
         _topk_case(x, 2048, ends, "adversarial bf16")
         torch.cuda.synchronize()

@@ -29,9 +29,11 @@ def _built():
 
 
 # (rows, cols, dtype, k, sorted): 9000 fp32 columns take one warp per row,
-# 16000 bf16 columns one CTA per row, 8 rows of 300000 a cluster per row
+# 16000 bf16 columns one CTA per row, 8 rows of 300000 a cluster per row;
+# score-sorted: 20001 columns on the CTA path, 8192 on the warp path
 ROW_CASES = [(64, 9000, torch.float32, 512, False), (16, 16000, torch.bfloat16, 512, False),
-             (8, 300000, torch.float32, 512, False), (12, 20001, torch.float32, 1000, True)]
+             (8, 300000, torch.float32, 512, False), (12, 20001, torch.float32, 1000, True),
+             (24, 8192, torch.float32, 512, True)]
 
 
 def _row_inputs(seed):
