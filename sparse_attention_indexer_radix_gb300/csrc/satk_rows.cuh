@@ -271,6 +271,25 @@ struct Group8<float, ALIGN> {
     for (int s = 0; s < 8; ++s) m |= (__uint_as_float(w[s]) >= t ? 1u : 0u) << s;
     return m;
   }
+  // the raw words to / from 32 bytes of shared memory (16-byte aligned)
+  __device__ __forceinline__ void stash(uint32_t *p) const {
+    reinterpret_cast<uint4 *>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  __device__ __forceinline__ void unstash(const uint32_t *p) {
+    const uint4 a = reinterpret_cast<const uint4 *>(p)[0];
+    const uint4 b = reinterpret_cast<const uint4 *>(p)[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+  // whether some element compares >= t (the maximum ignores NaN)
+  __device__ __forceinline__ bool any(float t) const {
+    const float a = fmaxf(fmaxf(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                          fmaxf(__uint_as_float(w[2]), __uint_as_float(w[3])));
+    const float b = fmaxf(fmaxf(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                          fmaxf(__uint_as_float(w[6]), __uint_as_float(w[7])));
+    return fmaxf(a, b) >= t;
+  }
 };
 
 template <int ALIGN>
@@ -301,6 +320,20 @@ struct Group8<uint16_t, ALIGN> {
       m |= ((h & 1u) | ((h >> 15) & 2u)) << (2 * j);
     }
     return m;
+  }
+  // the raw words to / from 16 bytes of shared memory (16-byte aligned)
+  __device__ __forceinline__ void stash(uint32_t *p) const {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ __forceinline__ void unstash(const uint32_t *p) {
+    const uint4 a = *reinterpret_cast<const uint4 *>(p);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  }
+  // whether some element compares >= t (the maximum ignores NaN)
+  __device__ __forceinline__ bool any(__nv_bfloat162 t2) const {
+    const __nv_bfloat162 *v = reinterpret_cast<const __nv_bfloat162 *>(w);
+    const __nv_bfloat162 m = __hmax2(__hmax2(v[0], v[1]), __hmax2(v[2], v[3]));
+    return __hge2_mask(m, t2) != 0u;
   }
 };
 
@@ -376,9 +409,12 @@ __device__ __forceinline__ void prefetch_row_head(const T *__restrict__ xr, int 
 // warp's loads (the first ones were requested before the threshold step).  Per-lane counts of each batch go
 // through one packed warp prefix scan.  The < 8 ragged columns at the end
 // go to the last warp.  Returns the segment; sets sm.flag on overflow.
+// (The element-wise form of collect_filtered, for stretches whose groups
+// mostly pass.)
 template <typename T, int BLOCK, int SUB, int ALIGN, int U>
-__device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int end, float t0f,
-                                                ListSmem<BLOCK, SUB> &sm, WarpStats &st) {
+__device__ __forceinline__ Seg collect_filtered_elems(const T *__restrict__ xr, int end,
+                                                      float t0f, ListSmem<BLOCK, SUB> &sm,
+                                                      WarpStats &st) {
   static_assert(U % 2 == 0, "counts are packed two per word");
   constexpr int NW = BLOCK / 32;
   constexpr int PF = 1;  // batches prefetched ahead (more is evicted before use)
@@ -465,6 +501,135 @@ __device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int en
   st.mn = __reduce_min_sync(kFull, kmn);
   st.mx = __reduce_max_sync(kFull, kmx);
   return Seg{warp * SUB, min(cnt, SUB)};
+}
+
+// The filtered pass for thresholds that keep few columns.  Every warp
+// streams its stretch of 8-element groups (one group per lane, U per lane
+// in flight, the copy engine a batch ahead) and tests each group by its
+// maximum against the threshold; a ballot stages the groups that pass --
+// their raw words in the warp's share of the idle histogram, their indices
+// in the last 32 entries of its list segment -- and each time 32 are
+// staged the warp takes them one per lane: the columns that compare >= the
+// threshold go, with their keys, to the list segment in column order
+// (per-lane counts through a warp prefix scan).  So the per-column work
+// runs only on passing groups, and nothing is read twice.  fp32 rows and an
+// unbounded threshold (every group passes) take collect_filtered_elems
+// instead.
+// The < 8 ragged columns at the end go to the last warp.  Returns the
+// segment; sets sm.flag on overflow.  The histogram is zero on entry and
+// on return.
+template <typename T, int BLOCK, int SUB, int ALIGN, int U>
+__device__ __forceinline__ Seg collect_filtered(const T *__restrict__ xr, int end, float t0f,
+                                                ListSmem<BLOCK, SUB> &sm, WarpStats &st) {
+  using G = Group8<T, ALIGN>;
+  constexpr int NW = BLOCK / 32;
+  constexpr int GW = sizeof(G::w) / sizeof(uint32_t);  // words per group
+  static_assert(32 * GW <= 2048 / NW, "32 staged groups per warp fit its histogram share");
+  constexpr int LCAP = SUB - 32;  // list entries; the last 32 hold staged indices
+  constexpr int PF = 1;           // batches prefetched ahead
+  const int lane = lane_id(), warp = warp_id();
+  const unsigned lt = (1u << lane) - 1u;
+  // fp32 rows stay on the element path: their 32-byte groups leave the
+  // staging loop short of registers (measured slower at 25600 - 102400
+  // columns), while bf16 rows gain
+  if (std::is_same<T, float>::value || !(t0f > __uint_as_float(0xff800000u)))
+    return collect_filtered_elems<T, BLOCK, SUB, ALIGN, U>(xr, end, t0f, sm, st);
+  const int ngroups = end / 8;
+  int g0, g1;
+  warp_stretch<BLOCK>(end, g0, g1);
+  uint32_t *stw = sm.sel.hist + warp * (2048 / NW);  // staged groups' words
+  uint32_t *lk = sm.key + warp * SUB;
+  uint32_t *lv = sm.val + warp * SUB;
+  uint32_t *sgi = lv + LCAP;  // staged groups' indices
+  const ThresholdOf<T> thr(t0f);
+  int cnt = 0, staged = 0;
+  bool over = false;  // warp-uniform: the list segment overflowed
+  uint32_t kmn = 0xffffffffu, kmx = 0u;  // range of the keys written
+  auto flush = [&]() {  // warp-uniform; the staged groups, one per lane
+    __syncwarp();
+    G grp;
+    uint32_t m = 0u;
+    int gi = 0;
+    if (lane < staged) {
+      grp.unstash(stw + lane * GW);
+      gi = static_cast<int>(sgi[lane]);
+      m = grp.mask(thr.arg());
+    }
+    const int lc = __popc(m);
+    const int incl = warp_incl_scan(lc);
+    const int tot = __shfl_sync(kFull, incl, 31);
+    if (cnt + tot > LCAP) {
+      over = true;
+    } else {
+      int pos = cnt + incl - lc;
+      const int c0 = gi * 8;
+      while (m != 0u) {
+        const int s = __ffs(m) - 1;
+        m &= m - 1u;
+        const uint32_t k = key_of_num<T>(grp.raw(s));
+        if (satk_check(pos < LCAP, kDbgList)) {
+          lk[pos] = k;
+          lv[pos] = static_cast<uint32_t>(c0 + s);
+        }
+        kmn = min(kmn, k);
+        kmx = max(kmx, k);
+        ++pos;
+      }
+    }
+    cnt += tot;
+    staged = 0;
+    __syncwarp();
+  };
+  for (int gb = g0; gb < g1 && !over; gb += 32 * U) {
+    prefetch_groups<T, ALIGN>(xr, min(g1, gb + PF * 32 * U), min(g1, gb + (PF + 1) * 32 * U));
+    G grp[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int gi = gb + u * 32 + lane;
+      if (gi < g1) grp[u].load(xr + static_cast<size_t>(gi) * 8);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int gi = gb + u * 32 + lane;
+      const bool p = gi < g1 && grp[u].any(thr.arg());
+      const unsigned b = __ballot_sync(kFull, p);
+      if (b != 0u) {  // warp-uniform
+        const int c = __popc(b);
+        if (staged + c > 32) flush();
+        if (p) {
+          const int slot = staged + __popc(b & lt);
+          grp[u].stash(stw + slot * GW);
+          sgi[slot] = static_cast<uint32_t>(gi);
+        }
+        staged += c;
+      }
+    }
+  }
+  if (staged != 0 && !over) flush();
+  __syncwarp();
+#pragma unroll
+  for (int w = lane; w < 32 * GW; w += 32) stw[w] = 0u;  // the histogram zero again
+  if (warp == NW - 1 && ngroups * 8 < end && !over) {  // ragged columns
+    const int c = ngroups * 8 + lane;
+    const uint32_t rw = c < end ? load_raw(xr + c) : 0u;
+    const bool keep = c < end && as_float<T>(rw) >= t0f;
+    const unsigned b = __ballot_sync(kFull, keep);
+    const int pos = cnt + __popc(b & lt);
+    if (keep && pos < LCAP) {
+      const uint32_t k = key_of_num<T>(rw);
+      lk[pos] = k;
+      lv[pos] = static_cast<uint32_t>(c);
+      kmn = min(kmn, k);
+      kmx = max(kmx, k);
+    }
+    cnt += __popc(b);
+    over = cnt > LCAP;
+  }
+  if (over && lane == 0) sm.flag = 1;
+  st.n = min(cnt, LCAP);
+  st.mn = __reduce_min_sync(kFull, kmn);
+  st.mx = __reduce_max_sync(kFull, kmx);
+  return Seg{warp * SUB, min(cnt, LCAP)};
 }
 
 // ------------------------------------------------------ exact (fallback) --
