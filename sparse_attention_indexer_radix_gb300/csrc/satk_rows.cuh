@@ -389,9 +389,22 @@ __device__ __forceinline__ void prefetch_groups(const T *__restrict__ xr, int ga
 }
 
 // Groups per lane per batch of the filtered pass, and samples per thread of
-// the threshold step.
+// the cluster path's threshold step (a slice there is only known to exceed
+// CAP - 8 columns, and the sample needs BLOCK * samples of them).
 constexpr int kRowBatch = 4;
 constexpr int kRowSample = 4;
+
+// Samples per thread of the CTA path's threshold step (its rows exceed CAP
+// >= BLOCK * 16 columns): a larger sample tightens the threshold, so the
+// list shrinks toward K, at the cost of its loads and histogram.  Measured
+// best: 8 for fp32 rows (4096 x 51200, K 512: 167 -> 164 us against 4; 16
+// was slower at 25600 columns) and 16 for bf16 rows (the decode top-384 pack
+// of 65536 columns: 50 -> 46 us against 4), whose small K per column left
+// the 4-sample threshold loosest.
+template <typename T>
+__host__ __device__ constexpr int row_sample() {
+  return sizeof(T) == 2 ? 16 : 8;
+}
 
 // L2 prefetch of the first two batches of every warp's stretch of a row of
 // `end` columns: what the filtered pass reads first.
@@ -847,6 +860,7 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
   constexpr int CAP = ListSmem<BLOCK, SUB>::CAP;
   constexpr bool VECLOAD = ALIGN != 0;
   constexpr int U = kRowBatch;
+  static_assert(CAP >= BLOCK * row_sample<T>(), "a sampled row (end > CAP) holds the sample");
   const bool all = end <= CAP;
   // start the copy engine on the first batches of this warp's stretch
   prefetch_row_head<T, BLOCK, ALIGN>(xr, end);
@@ -855,9 +869,9 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
     t0f = __uint_as_float(0xff800000u);  // -inf: every valid column
   } else {
     bool ok;
-    t0f = value_sample_threshold<T, BLOCK, kRowSample, SUB>(xr, end, K, sm, ok);
+    t0f = value_sample_threshold<T, BLOCK, row_sample<T>(), SUB>(xr, end, K, sm, ok);
     if (!ok)  // block-uniform
-      t0f = threshold_float<KB>(sample_threshold<T, BLOCK, kRowSample, SUB>(xr, end, K, sm));
+      t0f = threshold_float<KB>(sample_threshold<T, BLOCK, row_sample<T>(), SUB>(xr, end, K, sm));
   }
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear
