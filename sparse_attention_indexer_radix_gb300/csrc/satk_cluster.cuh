@@ -43,7 +43,8 @@ enum ClusterSlot : int {
   kPubMinAbove = 8,     // smallest key >= T
   kPubCountA = 9,       // entries above the K-th key
   kPubCountB = 10,      // entries equal to it
-  kPubSlots = 12
+  kPubSampleRange = 12, // smallest, largest sampled value (ordered ints)
+  kPubSlots = 14
 };
 
 template <int BLOCK, int SUB>
@@ -327,6 +328,107 @@ __device__ void cluster_topk_emit(cg::cluster_group &cl, ClusterSmem<BLOCK, SUB>
 }
 
 // The whole row on a cluster of C CTAs (this CTA is rank cl.block_rank()):
+// T0 of a row split over the cluster from the union of the C slices'
+// samples (kRowSample runs of 32 columns per warp, spread over each slice,
+// held in registers): the sampled values' range is exchanged once, every
+// CTA builds a value-linear 256-bin histogram of its own samples, and the
+// sum of the C histograms read through distributed shared memory gives the
+// bin of the r-th largest value (a finer round inside a bin holding more
+// than 32 samples); T0 is that bin's lower edge moved down by a few ulps,
+// on T's grid.  Three cluster barriers (five with the finer round) where
+// the ordered-key digits of the union take up to seven.  Every branch
+// depends only on cluster-wide values, so all CTAs take the same number of
+// barriers.  ok = false (cluster-uniform, after one barrier) when the
+// range is not usable (an infinity, a single value): the caller ranks the
+// samples by ordered keys.  -inf when fewer than r values are valid.  The
+// histogram is zero on entry and on return.
+template <typename T, int BLOCK, int SUB, int C>
+__device__ float cluster_value_threshold(cg::cluster_group &cl, const T *__restrict__ xs,
+                                         int send, int r, ClusterSmem<BLOCK, SUB> &cs,
+                                         bool &ok) {
+  constexpr int SPT = kRowSample;
+  constexpr int NW = BLOCK / 32;
+  constexpr int NRUNS = BLOCK * SPT / 32;
+  SelectSmem<BLOCK> &sel = cs.ls.sel;
+  const int lane = lane_id(), warp = warp_id();
+  float v[SPT];
+#pragma unroll
+  for (int q = 0; q < SPT; ++q) {
+    const int run = warp * SPT + q;
+    const int start = static_cast<int>((static_cast<int64_t>(run) * send) / NRUNS) & ~31;
+    v[q] = as_float<T>(load_raw(xs + start + lane));
+  }
+  float mn = __uint_as_float(0x7f800000u), mx = __uint_as_float(0xff800000u);
+#pragma unroll
+  for (int q = 0; q < SPT; ++q) {
+    mn = fminf(mn, v[q]);  // NaN ignored
+    mx = fmaxf(mx, v[q]);
+  }
+  const int wmn = __reduce_min_sync(kFull, float_order(mn));
+  const int wmx = __reduce_max_sync(kFull, float_order(mx));
+  if (lane == 0) {
+    sel.wtot[1][warp] = wmn;
+    sel.wtot[2][warp] = wmx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int bmn = sel.wtot[1][0], bmx = sel.wtot[2][0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+      bmn = min(bmn, sel.wtot[1][w]);
+      bmx = max(bmx, sel.wtot[2][w]);
+    }
+    cs.pub[kPubSampleRange] = static_cast<uint32_t>(bmn);
+    cs.pub[kPubSampleRange + 1] = static_cast<uint32_t>(bmx);
+  }
+  cl.sync();  // every CTA's range published
+  int imn = static_cast<int>(cluster_word(cl, &cs.pub[kPubSampleRange], 0));
+  int imx = static_cast<int>(cluster_word(cl, &cs.pub[kPubSampleRange + 1], 0));
+#pragma unroll
+  for (int c = 1; c < C; ++c) {
+    imn = min(imn, static_cast<int>(cluster_word(cl, &cs.pub[kPubSampleRange], c)));
+    imx = max(imx, static_cast<int>(cluster_word(cl, &cs.pub[kPubSampleRange + 1], c)));
+  }
+  mn = float_of_order(imn);
+  mx = float_of_order(imx);
+  ok = true;
+  const float ninf = __uint_as_float(0xff800000u);
+  if (mx < mn) return ninf;  // no valid sample in the row (cluster-uniform)
+  const float span = mx - mn;
+  if (!(span > 0.f) || !(span < __uint_as_float(0x7f800000u))) {  // cluster-uniform
+    ok = false;
+    return 0.f;
+  }
+  const float sc = 256.f * __frcp_rn(span);
+#pragma unroll
+  for (int q = 0; q < SPT; ++q)
+    if (v[q] == v[q]) atomicAdd(sel.hist + value_bin(v[q], mn, sc), 1u);
+  __syncthreads();
+  cl.sync();  // every CTA's histogram complete
+  const PassOut p = cluster_find_threshold<BLOCK, 256, C>(cl, sel, r);
+  cl.sync();  // every CTA done reading the histograms
+  for (int i = threadIdx.x; i < 256; i += BLOCK) sel.hist[i] = 0u;
+  __syncthreads();
+  if (p.d < 0) return ninf;  // fewer than r valid samples (cluster-uniform)
+  float t = mn + static_cast<float>(p.d) * __frcp_rn(sc);
+  if (p.cnt > 32 && p.d < 255) {  // cluster-uniform: a crowded bin, a finer round inside it
+    const float sc2 = sc * 256.f;
+    const float lo2 = t;
+#pragma unroll
+    for (int q = 0; q < SPT; ++q)
+      if (v[q] == v[q] && value_bin(v[q], mn, sc) == p.d)
+        atomicAdd(sel.hist + value_bin(v[q], lo2, sc2), 1u);
+    __syncthreads();
+    cl.sync();  // every CTA's finer histogram complete
+    const PassOut p2 = cluster_find_threshold<BLOCK, 256, C>(cl, sel, r - p.above);
+    cl.sync();  // every CTA done reading them
+    for (int i = threadIdx.x; i < 256; i += BLOCK) sel.hist[i] = 0u;
+    __syncthreads();
+    if (p2.d >= 0) t = lo2 + static_cast<float>(p2.d) * __frcp_rn(sc2);
+  }
+  return grid_floor<T>(t - fabsf(t) * 9.5367e-7f - 1e-37f);
+}
+
 // put(pos, key, column) for output position pos of the row's top-K layout
 // (the layout of topk_row), fill(pos) for the positions past the last
 // candidate.  The histogram must be zero on entry.
@@ -351,11 +453,15 @@ __device__ void cluster_topk_row(cg::cluster_group &cl, const T *__restrict__ xr
   prefetch_row_head<T, BLOCK, ALIGN>(xs, send);
   float t0f = __uint_as_float(0xff800000u);
   if (!all) {  // every slice has > CAP - 8 * C columns: enough for its sample
-    const Seg ss = sample_keys<T, BLOCK, kRowSample, SUB>(xs, send, sm);
     const int r = sample_rank(K, C * BLOCK * kRowSample, end);
-    const Sel s = cluster_list_select<BLOCK, SUB, C>(
-        cl, [&](int i) { return sm.key[i]; }, ss, r, cs, 3, kPubSampleStats);
-    t0f = threshold_float<KB>(s.take_all ? 1u : s.T);
+    bool ok;
+    t0f = cluster_value_threshold<T, BLOCK, SUB, C>(cl, xs, send, r, cs, ok);
+    if (!ok) {  // cluster-uniform: rank the samples by ordered keys
+      const Seg ss = sample_keys<T, BLOCK, kRowSample, SUB>(xs, send, sm);
+      const Sel s = cluster_list_select<BLOCK, SUB, C>(
+          cl, [&](int i) { return sm.key[i]; }, ss, r, cs, 3, kPubSampleStats);
+      t0f = threshold_float<KB>(s.take_all ? 1u : s.T);
+    }
   }
   if (threadIdx.x == 0) sm.flag = 0;
   __syncthreads();  // sample keys read, flag clear
