@@ -118,12 +118,13 @@ __device__ __forceinline__ PassOut cluster_find_threshold(cg::cluster_group &cl,
 
 // list_select (satk_list.cuh) over the union of the C CTAs' lists: the K
 // largest of the non-zero keys gk(i) of every CTA's segments.  `slot` is
-// the first of three pub slots for the count and key range.  Identical
-// result in every CTA of the cluster.
+// the first of three pub slots for the count and key range; lz, the low
+// key bits known to be zero (bf16 keys).  Identical result in every CTA of
+// the cluster.
 template <int BLOCK, int SUB, int C, class GetKey>
 __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &sg, int K,
                                    ClusterSmem<BLOCK, SUB> &cs, int max_passes, int slot,
-                                   WarpStats pre = stats_unknown()) {
+                                   WarpStats pre = stats_unknown(), int lz = 0) {
   SelectSmem<BLOCK> &sm = cs.ls.sel;
   const int lane = lane_id();
   uint32_t mn = 0xffffffffu, mx = 0u;
@@ -184,7 +185,7 @@ __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &
     r.need = 0;
     return r;
   }
-  const uint32_t span = mx - mn;
+  const uint32_t span = (mx - mn) >> lz;
   const int b = span == 0u ? 0 : 32 - __clz(span);
   int need = K;
   uint32_t prefix = 0u;
@@ -201,7 +202,7 @@ __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &
       const int i = j * 32 + lane;
       const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
       if (k != 0u) {
-        const uint32_t rel = k - mn;
+        const uint32_t rel = (k - mn) >> lz;
         if (pbits == 0 || (rel >> (shift + width)) == prefix)
           atomicAdd(sm.hist + ((rel >> shift) & dmask), 1u);
       }
@@ -215,12 +216,12 @@ __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &
     prefix = (prefix << width) | static_cast<uint32_t>(p.d);
     pbits += width;
     if (p.cnt == need || --max_passes == 0) {
-      r.T = mn + (prefix << shift);
+      r.T = mn + ((prefix << shift) << lz);
       r.need = need;
       return r;
     }
   }
-  r.T = mn + prefix;
+  r.T = mn + (prefix << lz);
   r.need = need;
   r.tie = true;
   return r;
@@ -234,13 +235,14 @@ __device__ Sel cluster_list_select(cg::cluster_group &cl, GetKey gk, const Seg &
 template <int BLOCK, int SUB, int C, class Put, class Fill>
 __device__ void cluster_topk_emit(cg::cluster_group &cl, ClusterSmem<BLOCK, SUB> &cs,
                                   const Seg &sg, int K, int col0, Put put, Fill fill,
-                                  WarpStats pre) {
+                                  WarpStats pre, int lz) {
   ListSmem<BLOCK, SUB> &sm = cs.ls;
   const int crank = static_cast<int>(cl.block_rank());
   const int lane = lane_id();
   const unsigned lt = (1u << lane) - 1u;
   auto gk = [&](int i) { return sm.key[i]; };
-  const Sel sel = cluster_list_select<BLOCK, SUB, C>(cl, gk, sg, K, cs, 8, kPubListStats, pre);
+  const Sel sel =
+      cluster_list_select<BLOCK, SUB, C>(cl, gk, sg, K, cs, 8, kPubListStats, pre, lz);
   uint32_t v;
   if (sel.take_all) {
     v = 0u;  // every entry is above
@@ -459,7 +461,8 @@ __device__ void cluster_topk_row(cg::cluster_group &cl, const T *__restrict__ xr
     if (!ok) {  // cluster-uniform: rank the samples by ordered keys
       const Seg ss = sample_keys<T, BLOCK, kRowSample, SUB>(xs, send, sm);
       const Sel s = cluster_list_select<BLOCK, SUB, C>(
-          cl, [&](int i) { return sm.key[i]; }, ss, r, cs, 3, kPubSampleStats);
+          cl, [&](int i) { return sm.key[i]; }, ss, r, cs, 3, kPubSampleStats, stats_unknown(),
+          32 - KB);
       t0f = threshold_float<KB>(s.take_all ? 1u : s.T);
     }
   }
@@ -482,7 +485,7 @@ __device__ void cluster_topk_row(cg::cluster_group &cl, const T *__restrict__ xr
     total += static_cast<int>(cluster_word(cl, &cs.pub[kPubCount], c));
   }
   if (!over && (all || total >= K)) {  // cluster-uniform
-    cluster_topk_emit<BLOCK, SUB, C>(cl, cs, sg, K, col0, put, fill, st);
+    cluster_topk_emit<BLOCK, SUB, C>(cl, cs, sg, K, col0, put, fill, st, 32 - KB);
   } else if (crank == 0) {  // the exact path, on CTA 0 over the whole row
     __syncthreads();
     sg = collect_exact<T, BLOCK, SUB, VECLOAD>(xr, end, K, sm);
@@ -491,7 +494,7 @@ __device__ void cluster_topk_row(cg::cluster_group &cl, const T *__restrict__ xr
         [&](int pos, int i) {
           if ((unsigned)pos < (unsigned)K) put(pos, sm.key[i], static_cast<int>(sm.val[i]));
         },
-        fill);
+        fill, stats_unknown(), 32 - KB);
   }
   cl.sync();  // no CTA leaves while another may still read its shared memory
 }

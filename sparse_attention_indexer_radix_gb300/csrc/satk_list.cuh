@@ -67,10 +67,12 @@ constexpr int kListFinish = 64;
 // With max_passes, the digit passes stop early and T is the start of the
 // threshold digit (at least K keys are >= T).  With pre known, the warp's
 // count and key range come from the caller instead of a walk over the list
-// (gk must then be non-zero exactly on those entries).
+// (gk must then be non-zero exactly on those entries).  With lz, the low lz
+// bits of every key are known to be zero (bf16 keys: ord16 << 16), so the
+// digits start above them.
 template <int BLOCK, class GetKey>
 __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &sm,
-                           int max_passes = 8, WarpStats pre = stats_unknown()) {
+                           int max_passes = 8, WarpStats pre = stats_unknown(), int lz = 0) {
   const int lane = lane_id();
   uint32_t mn = 0xffffffffu, mx = 0u;
   int n = 0;
@@ -114,7 +116,7 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
   r.tie = false;
   r.take_all = false;
   r.total = total;
-  const uint32_t span = mx - mn;
+  const uint32_t span = (mx - mn) >> lz;
   const int b = span == 0u ? 0 : 32 - __clz(span);
   if (total < K || b == 0) __syncthreads();  // no pass barrier follows
   if (total < K) {
@@ -141,7 +143,7 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
       const int i = j * 32 + lane;
       const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
       if (k != 0u) {
-        const uint32_t rel = k - mn;
+        const uint32_t rel = (k - mn) >> lz;
         if (pbits == 0 || (rel >> (shift + width)) == prefix)
           atomicAdd(sm.hist + ((rel >> shift) & dmask), 1u);
       }
@@ -154,7 +156,7 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
     prefix = (prefix << width) | static_cast<uint32_t>(p.d);
     pbits += width;
     if (p.cnt == need) {
-      r.T = mn + (prefix << shift);
+      r.T = mn + ((prefix << shift) << lz);
       r.need = need;
       return r;
     }
@@ -164,7 +166,7 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
       for (int j = 0; j < sg.rounds(); ++j) {
         const int i = j * 32 + lane;
         const uint32_t k = i < sg.cnt ? gk(sg.base + i) : 0u;
-        if (k != 0u && ((k - mn) >> shift) == prefix) {
+        if (k != 0u && (((k - mn) >> lz) >> shift) == prefix) {
           const int pos = atomicAdd(&sm.fcnt, 1);
           if (pos < kListFinish) sm.fin[pos] = k;
         }
@@ -209,14 +211,14 @@ __device__ Sel list_select(GetKey gk, const Seg &sg, int K, SelectSmem<BLOCK> &s
       return r;
     }
     if (--max_passes == 0) {
-      r.T = mn + (prefix << shift);
+      r.T = mn + ((prefix << shift) << lz);
       r.need = need;
       return r;
     }
   }
   // every key bit resolved: the K-th key is mn + prefix and `need` of the
   // keys equal to it are still wanted (more than need share it)
-  r.T = mn + prefix;
+  r.T = mn + (prefix << lz);
   r.need = need;
   r.tie = true;
   return r;
@@ -309,11 +311,12 @@ __device__ int list_emit1(SelF sel, const Seg &sg, Emit emit, SelectSmem<BLOCK> 
 
 // Row top-K layout from the list: entries above the K-th key in list order,
 // then entries equal to it in list order up to K, then fill(pos) up to K.
+// lz: low key bits known to be zero (list_select).
 template <int BLOCK, int SUB, class Put, class Fill>
 __device__ void list_topk_emit(ListSmem<BLOCK, SUB> &sm, const Seg &sg, int K, Put put,
-                               Fill fill, WarpStats pre = stats_unknown()) {
+                               Fill fill, WarpStats pre = stats_unknown(), int lz = 0) {
   auto gk = [&](int i) { return sm.key[i]; };
-  const Sel sel = list_select<BLOCK>(gk, sg, K, sm.sel, 8, pre);
+  const Sel sel = list_select<BLOCK>(gk, sg, K, sm.sel, 8, pre, lz);
   uint32_t v;
   if (sel.take_all) {
     v = 0u;

@@ -885,7 +885,8 @@ __device__ void topk_row(const T *__restrict__ xr, int end, int K, Put put, Fill
     __syncthreads();
     sg = collect_exact<T, BLOCK, SUB, VECLOAD>(xr, end, K, sm);
   }
-  list_topk_emit<BLOCK, SUB>(sm, sg, K, put, fill, ok ? st : stats_unknown());
+  // bf16 keys are ord16 << 16: their low 16 bits are zero
+  list_topk_emit<BLOCK, SUB>(sm, sg, K, put, fill, ok ? st : stats_unknown(), 32 - KB);
 }
 
 }  // namespace satk
