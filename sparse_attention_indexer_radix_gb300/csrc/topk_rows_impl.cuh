@@ -206,31 +206,31 @@ int launch_cluster(const T *x, int64_t rows, int cols, int64_t ld, const int32_t
   return launch_status();
 }
 
-// Cluster size for `rows` rows when one CTA per row would fill fewer than
-// three waves of resident CTAs (0: no cluster): the smallest of 2, 4, 8
-// that reaches three waves, else 8.  A cluster adds barriers to every step
-// of a row, which only pays when the slices stay long: with at least one
-// full wave of rows, a slice under kClusterMinSlice bytes keeps one CTA per
-// row (measured: 1024 bf16 rows of 128 KB ran 2x slower on two-CTA
-// clusters, 1310 fp32 rows of 400 KB 1.35x faster, 256 bf16 rows of up to
-// 256 KB 3.2x faster on eight).
-constexpr int64_t kClusterMinSlice = 128 * 1024;
-
+// Cluster size for `rows` rows when one CTA per row would not fill one wave
+// of resident CTAs (0: no cluster): the smallest of 2, 4, 8 whose clusters
+// fill a wave, else 8.  A cluster adds barriers to every step of a row,
+// which pays only while SMs would otherwise sit idle, and the fewer CTAs
+// share a row the fewer remote reads each barrier round costs (measured on
+// the current kernels: 1310 fp32 rows of 400 KB, 2.15 waves, 142.6 us on
+// two-CTA clusters against 118.3 us one CTA per row; 256 bf16 rows of 256 KB
+// with K = 2048, 0.56 waves, 52.5 us on two-CTA clusters against 114 us on
+// eight; four rows of 524288 columns take eight).
 template <typename T, int BLOCK, int SUB, int ALIGN>
 int cluster_size(int64_t rows, int cols) {
   if (rows > INT32_MAX / 8 || cols < 8 * 2 * ListSmem<BLOCK, SUB>::CAP) return 0;
+  // the occupancy query counts the shared memory only once the kernel may
+  // take it (above 48 KB)
+  auto kern = topk_rows_kernel<T, BLOCK, SUB, ALIGN>;
+  if (!allow_smem(kern, sizeof(ListSmem<BLOCK, SUB>))) return 0;
   const int64_t resident =
-      resident_ctas(reinterpret_cast<const void *>(topk_rows_kernel<T, BLOCK, SUB, ALIGN>),
-                    BLOCK, sizeof(ListSmem<BLOCK, SUB>));
-  if (resident <= 0 || rows >= 3 * resident) return 0;
+      resident_ctas(reinterpret_cast<const void *>(kern), BLOCK, sizeof(ListSmem<BLOCK, SUB>));
+  if (resident <= 0 || rows >= resident) return 0;
   int c = 8;
   for (int t = 2; t < 8; t *= 2)
-    if (rows * t >= 3 * resident) {
+    if (rows * t >= resident) {
       c = t;
       break;
     }
-  const int64_t slice = static_cast<int64_t>(cols) * static_cast<int64_t>(sizeof(T)) / c;
-  if (rows >= resident && slice < kClusterMinSlice) return 0;
   return c;
 }
 

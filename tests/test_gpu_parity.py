@@ -147,14 +147,18 @@ def test_topk_warp_rows_edges(dtype, ld):
         assert_rows_equal(got, want, f"warp rows {dtype} ld={ld} k={k}")
 
 
-@pytest.mark.parametrize("rows,dtype,ld", [(8, torch.float32, 70000), (600, torch.float32, 70000),
+@pytest.mark.parametrize("rows,dtype,ld", [(8, torch.float32, 70000), (200, torch.bfloat16, 70000),
+                                           (600, torch.float32, 70000),
                                            (1000, torch.float32, 70004),
                                            (600, torch.bfloat16, 70001)])
 def test_topk_few_long_rows(rows, dtype, ld):
-    """Few long rows (a cluster of CTAs per row: 8, 600 and 1000 rows take
-    different cluster sizes): random row ends around the slice and list
-    sizes, NaN, constant and few-level rows (the exact path), fp32 and bf16,
-    aligned and unaligned rows; sampled rows against the oracle."""
+    """Few long rows: rows that fill less than a wave of resident CTAs take
+    a cluster per row, the smallest of 2, 4, 8 CTAs whose clusters fill one
+    (8 rows: eight; 200: four; 600: two at K <= 1024, where 608 CTAs are
+    resident, one CTA per row at K = 2048), more rows one CTA per row (1000).
+    Random row ends around the slice and list sizes, NaN, constant and
+    few-level rows (the exact path), fp32 and bf16, aligned and unaligned
+    rows; sampled rows against the oracle."""
     cols = 70000
     x, _ = inputs.prefill(rows=rows, cols=cols, seed=rows + ld, dtype=torch.float32)
     g = torch.Generator().manual_seed(rows)
