@@ -295,13 +295,14 @@ __device__ void bitonic_sort_desc(uint64_t *buf) {
 
 // ---- score-sorted on one warp (short rows)
 //
-// The warp path's ordered emit records, for every output position, the
-// list index of the entry chosen there (a 16-bit map of P = 32 E entries,
-// 0xFFFF where no candidate).  The warp then gathers the chosen entries as
-// (key << 32 | ~column) composites into registers -- entry e * 32 + l in
-// lane l -- after which the list area is free for the sort's scratch:
+// The warp path's ordered emit records, for every output position below
+// K, the list index of the entry chosen there (a 16-bit map in the warp's
+// histogram words, 0xFFFF where no candidate).  The warp then gathers the
+// chosen entries as (key << 32 | ~column) composites into registers --
+// entry e * 32 + l in lane l, P = 32 E of them -- after which the list area
+// is free for the sort's scratch:
 //  - bucket sort (the usual case): bucket b(key) = floor((key - kmin) *
-//    P / (span + 1)) is monotone in the key, so with buckets taken from
+//    256 / (span + 1)) is monotone in the key, so with buckets taken from
 //    the highest down an entry's output position is the count of entries
 //    in higher buckets plus its rank by composite (key desc, column asc)
 //    among its own bucket's entries, counted by a walk over the bucket;
@@ -377,14 +378,14 @@ __device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[E]) {
   }
 }
 
-// The bucket sort over NB = 32 E buckets: composites c (0: no entry),
+// The bucket sort over NB = 256 buckets: composites c (0: no entry),
 // scratch tmp (32 E values), ranked columns to cols[0, n), hist (NB words)
 // zero on entry.  Returns n, the count of entries, or -1 (nothing written)
 // when a bucket holds more than 32 entries.
 template <int E>
 __device__ int warp_bucket_rank(const uint64_t (&c)[E], uint64_t *tmp, int32_t *cols,
                                 uint32_t *hist) {
-  constexpr int NB = 32 * E;
+  constexpr int NB = 256;
   const int lane = lane_id();
   uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
@@ -408,11 +409,12 @@ __device__ int warp_bucket_rank(const uint64_t (&c)[E], uint64_t *tmp, int32_t *
     if (c[e] != 0u) atomicAdd(hist + d[e], 1u);
   }
   __syncwarp();
-  // exclusive prefix over the buckets: lane l owns buckets E l .. E l + E - 1
-  uint32_t h[E], run = 0u, big = 0u;
+  // exclusive prefix over the buckets: lane l owns buckets BPL l .. BPL l + BPL - 1
+  constexpr int BPL = NB / 32;
+  uint32_t h[BPL], run = 0u, big = 0u;
 #pragma unroll
-  for (int j = 0; j < E; ++j) {
-    h[j] = hist[E * lane + j];
+  for (int j = 0; j < BPL; ++j) {
+    h[j] = hist[BPL * lane + j];
     run += h[j];
     big = max(big, h[j]);
   }
@@ -422,8 +424,8 @@ __device__ int warp_bucket_rank(const uint64_t (&c)[E], uint64_t *tmp, int32_t *
   __syncwarp();
   if (big > 32u) return -1;  // warp-uniform
 #pragma unroll
-  for (int j = 0; j < E; ++j) {
-    hist[E * lane + j] = base;
+  for (int j = 0; j < BPL; ++j) {
+    hist[BPL * lane + j] = base;
     base += h[j];
   }
   __syncwarp();
@@ -459,10 +461,11 @@ __device__ int warp_bucket_rank(const uint64_t (&c)[E], uint64_t *tmp, int32_t *
   return static_cast<int>(n);
 }
 
-// Six CTAs per SM: the sort's per-warp words push seven past the shared
-// memory.
+// Seven CTAs per SM, as the unsorted warp kernel: the index map lives in
+// the warp's histogram (idle and zero while the emit runs), and the bucket
+// counters reuse it after the gather.
 template <typename T, int ALIGN, int E>
-__global__ void __launch_bounds__(32 * kWarpRowsPerCta, 6)
+__global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
     topk_rows_warp_sorted_kernel(const T *__restrict__ x, int64_t rows, int64_t ld, int cols,
                                  const int32_t *__restrict__ row_ends, int K,
                                  int32_t *__restrict__ out, int64_t ld_out) {
@@ -474,14 +477,11 @@ __global__ void __launch_bounds__(32 * kWarpRowsPerCta, 6)
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpRowsPerCta + warp;
   if (row >= rows) return;  // warp-uniform; the warps never synchronise
   WarpRowSmem &ws = reinterpret_cast<WarpRowSmem *>(smem_raw)[warp];
-  // per warp 32 E words: the index map (16-bit) during the row, the bucket
-  // counters after it
-  uint32_t *aux = reinterpret_cast<uint32_t *>(smem_raw + sizeof(WarpRowSmem) * kWarpRowsPerCta) +
-                  warp * 32 * E;
+  // the emit writes map[pos] for every pos < K (no fill needed before the
+  // row: the histogram must be zero then)
+  uint32_t *aux = ws.hist;
   uint16_t *map = reinterpret_cast<uint16_t *>(aux);
   for (int i = lane; i < 256; i += 32) ws.hist[i] = 0u;
-#pragma unroll
-  for (int e = 0; e < E; ++e) map[e * 32 + lane] = 0xffffu;  // positions past K: none
   __syncwarp();
   warp_topk_row<T, ALIGN>(x + row * ld, row_end_of(row_ends, row, cols), K, SortMapOut{map, K},
                           ws);
@@ -489,14 +489,14 @@ __global__ void __launch_bounds__(32 * kWarpRowsPerCta, 6)
   uint64_t c[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const uint32_t i = map[e * 32 + lane];
+    const int p = e * 32 + lane;
+    const uint32_t i = p < K ? map[p] : 0xffffu;
     c[e] = i == 0xffffu ? 0u
                         : (static_cast<uint64_t>(ws.key()[i]) << 32) |
                               (0xffffffffu - static_cast<uint32_t>(ws.col()[i]));
   }
   __syncwarp();  // the list and the map are read: their areas are the sort's scratch now
-#pragma unroll
-  for (int e = 0; e < E; ++e) aux[e * 32 + lane] = 0u;
+  for (int i = lane; i < 256; i += 32) aux[i] = 0u;
   __syncwarp();
   uint64_t *tmp = reinterpret_cast<uint64_t *>(ws.buf);
   int32_t *ranked = reinterpret_cast<int32_t *>(tmp + 32 * E);
@@ -519,7 +519,7 @@ template <typename T, int ALIGN, int E>
 int launch_warp_sorted(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends,
                        int K, int32_t *out, int64_t ld_out, cudaStream_t st) {
   auto kern = topk_rows_warp_sorted_kernel<T, ALIGN, E>;
-  const size_t smem = (sizeof(WarpRowSmem) + sizeof(uint32_t) * 32 * E) * kWarpRowsPerCta;
+  const size_t smem = sizeof(WarpRowSmem) * kWarpRowsPerCta;
   if (!allow_smem(kern, smem)) return SATK_ECUDA;
   const int64_t grid = (rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta;
   kern<<<dim3(static_cast<unsigned>(grid)), 32 * kWarpRowsPerCta, smem, st>>>(
