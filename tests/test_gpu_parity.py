@@ -168,6 +168,9 @@ def test_topk_few_long_rows(rows, dtype, ld):
         ends[r] = e
     x[1] = float("nan")
     x[2, ::2] = float("nan")
+    if rows == 8:  # the cluster threshold's ordered-key fallback on eight-CTA clusters
+        x[6, ::97] = float("inf")                             # an infinity in the range
+        x[7] = 0.5                                            # a single value
     if rows > 8:
         for r, e in enumerate((8176, 8177, 16368, 16369, 32736, 65472, 65473), start=11):
             ends[r] = e                                       # list-size boundaries
