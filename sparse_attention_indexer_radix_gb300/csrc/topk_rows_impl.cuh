@@ -302,7 +302,7 @@ __device__ void bitonic_sort_desc(uint64_t *buf) {
 // entry e * 32 + l in lane l, P = 32 E of them -- after which the list area
 // is free for the sort's scratch:
 //  - bucket sort (the usual case): bucket b(key) = floor((key - kmin) *
-//    256 / (span + 1)) is monotone in the key, so with buckets taken from
+//    512 / (span + 1)) is monotone in the key, so with buckets taken from
 //    the highest down an entry's output position is the count of entries
 //    in higher buckets plus its rank by composite (key desc, column asc)
 //    among its own bucket's entries, counted by a walk over the bucket;
@@ -378,14 +378,14 @@ __device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[E]) {
   }
 }
 
-// The bucket sort over NB = 256 buckets: composites c (0: no entry),
-// scratch tmp (32 E values), ranked columns to cols[0, n), hist (NB words)
-// zero on entry.  Returns n, the count of entries, or -1 (nothing written)
+// The bucket sort over NB = 512 buckets: composites c (0: no entry),
+// scratch tmp (32 E values), ranked columns to cols[0, n) (the output row),
+// hist (NB words) zero on entry.  Returns n, the count of entries, or -1 (nothing written)
 // when a bucket holds more than 32 entries.
 template <int E>
 __device__ int warp_bucket_rank(const uint64_t (&c)[E], uint64_t *tmp, int32_t *cols,
                                 uint32_t *hist) {
-  constexpr int NB = 256;
+  constexpr int NB = 512;
   const int lane = lane_id();
   uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
@@ -462,16 +462,17 @@ __device__ int warp_bucket_rank(const uint64_t (&c)[E], uint64_t *tmp, int32_t *
 }
 
 // Seven CTAs per SM, as the unsorted warp kernel: the index map lives in
-// the warp's histogram (idle and zero while the emit runs), and the bucket
-// counters reuse it after the gather.
+// the warp's histogram (idle and zero while the emit runs); after the
+// gather the list area holds the scatter scratch and the 512 bucket
+// counters, and the ranked columns go straight to the output row.
 template <typename T, int ALIGN, int E>
 __global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
     topk_rows_warp_sorted_kernel(const T *__restrict__ x, int64_t rows, int64_t ld, int cols,
                                  const int32_t *__restrict__ row_ends, int K,
                                  int32_t *__restrict__ out, int64_t ld_out) {
-  static_assert(sizeof(uint64_t) * 32 * E + sizeof(int32_t) * 32 * E <=
-                    sizeof(WarpRowSmem::buf),
-                "the sort scratch must fit the list area");
+  static_assert(sizeof(uint64_t) * 32 * E <= 1024 * sizeof(uint32_t) &&
+                    (1024 + 512) * sizeof(uint32_t) <= sizeof(WarpRowSmem::buf),
+                "the scatter scratch and the 512 bucket counters fit the list area");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int warp = warp_id(), lane = lane_id();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpRowsPerCta + warp;
@@ -479,8 +480,7 @@ __global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
   WarpRowSmem &ws = reinterpret_cast<WarpRowSmem *>(smem_raw)[warp];
   // the emit writes map[pos] for every pos < K (no fill needed before the
   // row: the histogram must be zero then)
-  uint32_t *aux = ws.hist;
-  uint16_t *map = reinterpret_cast<uint16_t *>(aux);
+  uint16_t *map = reinterpret_cast<uint16_t *>(ws.hist);
   for (int i = lane; i < 256; i += 32) ws.hist[i] = 0u;
   __syncwarp();
   warp_topk_row<T, ALIGN>(x + row * ld, row_end_of(row_ends, row, cols), K, SortMapOut{map, K},
@@ -495,15 +495,15 @@ __global__ void __launch_bounds__(32 * kWarpRowsPerCta, 7)
                         : (static_cast<uint64_t>(ws.key()[i]) << 32) |
                               (0xffffffffu - static_cast<uint32_t>(ws.col()[i]));
   }
-  __syncwarp();  // the list and the map are read: their areas are the sort's scratch now
-  for (int i = lane; i < 256; i += 32) aux[i] = 0u;
-  __syncwarp();
+  __syncwarp();  // the list and the map are read: the list area is the sort's scratch now
   uint64_t *tmp = reinterpret_cast<uint64_t *>(ws.buf);
-  int32_t *ranked = reinterpret_cast<int32_t *>(tmp + 32 * E);
+  uint32_t *cnt512 = ws.buf + 1024;  // the list area's last 2 KB: the bucket counters
+  for (int i = lane; i < 512; i += 32) cnt512[i] = 0u;
+  __syncwarp();
   int32_t *o = out + row * ld_out;
-  const int nb = warp_bucket_rank<E>(c, tmp, ranked, aux);
+  const int nb = warp_bucket_rank<E>(c, tmp, o, cnt512);
   if (nb >= 0) {  // warp-uniform
-    for (int q = lane; q < K; q += 32) o[q] = q < nb ? ranked[q] : -1;
+    for (int q = nb + lane; q < K; q += 32) o[q] = -1;
     return;
   }
   warp_bitonic_desc<E>(c);
