@@ -288,6 +288,14 @@ def test_prefill_full_size_every_row(cols):
     check_full_size(x, ends, inputs.PREFILL_LD_OUT, what=f"prefill {cols}")
 
 
+def test_prefill_sorted_full_size_every_row():
+    """The score-sorted option on the prefill 8192-column width at full size
+    (4096 rows, K = 512, the benchmark's workload; one warp per row and the
+    bucket sort): every row against the oracle's score order."""
+    x, ends = inputs.prefill(rows=inputs.PREFILL_ROWS, cols=8192, seed=1236, device=DEV)
+    check_full_size(x, ends, inputs.PREFILL_LD_OUT, what="sorted 8192", sorted=True)
+
+
 @pytest.mark.parametrize("rows,cols", [(8192, 4096), (8192, 8192), (2048, 25600), (2048, 51200),
                                        (1310, 102400)])
 def test_prefill_page_shapes_every_row(rows, cols):
@@ -305,18 +313,19 @@ def test_prefill_shifted_full_size_every_row(mode):
     check_full_size(x, ends, inputs.PREFILL_K, what=mode)
 
 
-def check_full_size(x, ends, ld_out, what, chunk=1024):
+def check_full_size(x, ends, ld_out, what, chunk=1024, sorted=False):
     """Every row of a full-size launch against the oracle, canaries past K
     included (the oracle runs in row chunks to bound host memory)."""
     rows, k = x.shape[0], inputs.PREFILL_K
     out = torch.full((rows, ld_out), CANARY, dtype=torch.int32, device=DEV)
-    satk.topk_rows(x, k, row_ends=ends, out=out)
+    satk.topk_rows(x, k, row_ends=ends, out=out, sorted=sorted)
     got = out.cpu().numpy()
     ends_h = ends.cpu().numpy()
     for r0 in range(0, rows, chunk):
         r1 = min(rows, r0 + chunk)
         want = np.full((r1 - r0, ld_out), CANARY, dtype=np.int32)
-        oracle.topk_rows(x[r0:r1].cpu().numpy(), k, row_ends=ends_h[r0:r1], out=want)
+        oracle.topk_rows(x[r0:r1].cpu().numpy(), k, row_ends=ends_h[r0:r1], out=want,
+                         sorted=sorted)
         assert_rows_equal(got[r0:r1], want, f"{what} rows {r0}..{r1}")
     # every row (N(0,1): no NaN): min(end, k) ids in [0, end), unique, then
     # -1, canaries intact
