@@ -26,12 +26,13 @@
 namespace satk {
 namespace {
 
-// 256 threads per row; rows of at most 16384 columns with K <= 512 take
-// 128 (more rows resident per SM, shorter barriers: short rows are bound by
-// the per-row select, not by the stream).
+// 256 threads per row; rows whose sampled list fits the smaller list with
+// room to spare (short_cta_rows_fit) take 128 (more rows resident per SM,
+// shorter barriers: short rows are bound by the per-row select, not by the
+// stream).
 constexpr int kBlock = 256;
 constexpr int kShortBlock = 128;
-constexpr int kShortCols = 16384;
+constexpr int kShortCols = 24576;
 
 __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, int cols) {
   if (row_ends == nullptr) return cols;
@@ -252,13 +253,34 @@ int launch_rows_cta(const T *x, int64_t rows, int cols, int64_t ld, const int32_
   }
 }
 
+// Whether rows of `cols` columns take the 128-thread CTA: its list (four
+// warps x 512 entries) must hold the sampled list -- K r / mu entries with
+// mu = K x samples / cols and r as in the sample step, samples = 128 x
+// row_sample<T>() -- plus four standard deviations (about list / sqrt(r))
+// within 80 % of its capacity, because a warp segment that overflows sends
+// its row to the exact pass, which in a launch of several waves can outlast
+// the whole launch.  Measured on 4096 causal fp32 rows at K = 512, 128
+// against 256 threads: 18432 columns 97 -> 87 us, 20480 103 -> 93 us;
+// at 35840 columns two rows overflowed and the launch took 223 us against
+// 134 us.  Rows above kShortCols stay on 256 threads whatever the estimate.
+template <typename T>
+inline bool short_cta_rows_fit(int cols, int K) {
+  constexpr int CAP = ListSmem<kShortBlock, 512>::CAP;
+  if (K > 512 || cols > kShortCols) return false;
+  if (cols <= CAP) return true;
+  const double mu = static_cast<double>(K) * kShortBlock * row_sample<T>() / cols;
+  const double r = std::ceil(mu + 4.0 * std::sqrt(mu) + 4.0);
+  const double list = K * r / mu;
+  return list + 4.0 * list / std::sqrt(r) <= 0.8 * CAP;
+}
+
 // The list holds (BLOCK/32) warps x SUB candidates.
 template <typename T, int ALIGN, class Out = IdOut>
 int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *row_ends, int K,
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
   if (warp_rows_fit(cols, K))
     return launch_warp<T, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
-  if (cols <= kShortCols && K <= 512)
+  if (short_cta_rows_fit<T>(cols, K))
     return launch<T, kShortBlock, 512, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out, ld_out,
                                                    st);
   if (K <= 1024)

@@ -79,7 +79,8 @@ def test_prefill_smoke_workload():
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("cols", [37, 1000, 2048, 2049, 4100, 8191, 8192, 9000, 16390, 40000])
+@pytest.mark.parametrize("cols", [37, 1000, 2048, 2049, 4100, 8191, 8192, 9000, 16390, 22528,
+                                  24576, 40000])
 def test_topk_shapes_both_paths(dtype, cols):
     rows = 24
     x, _ = inputs.prefill(rows=rows, cols=cols, seed=cols, dtype=dtype)
