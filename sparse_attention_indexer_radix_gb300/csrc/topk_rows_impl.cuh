@@ -32,7 +32,11 @@ namespace {
 // stream).
 constexpr int kBlock = 256;
 constexpr int kShortBlock = 128;
-constexpr int kShortCols = 24576;
+// the widest rows measured faster on 128 threads: fp32 and bf16
+template <typename T>
+constexpr int short_cols_max() {
+  return sizeof(T) == 2 ? 45056 : 24576;
+}
 
 __device__ __forceinline__ int row_end_of(const int32_t *row_ends, int64_t row, int cols) {
   if (row_ends == nullptr) return cols;
@@ -262,11 +266,13 @@ int launch_rows_cta(const T *x, int64_t rows, int cols, int64_t ld, const int32_
 // the whole launch.  Measured on 4096 causal fp32 rows at K = 512, 128
 // against 256 threads: 18432 columns 97 -> 87 us, 20480 103 -> 93 us;
 // at 35840 columns two rows overflowed and the launch took 223 us against
-// 134 us.  Rows above kShortCols stay on 256 threads whatever the estimate.
+// 134 us.  bf16 rows (16 samples per thread) fit wider rows: 30720 columns
+// 101 -> 91 us, 43008 115 -> 108 us.  Rows above short_cols_max<T>() stay
+// on 256 threads whatever the estimate.
 template <typename T>
 inline bool short_cta_rows_fit(int cols, int K) {
   constexpr int CAP = ListSmem<kShortBlock, 512>::CAP;
-  if (K > 512 || cols > kShortCols) return false;
+  if (K > 512 || cols > short_cols_max<T>()) return false;
   if (cols <= CAP) return true;
   const double mu = static_cast<double>(K) * kShortBlock * row_sample<T>() / cols;
   const double r = std::ceil(mu + 4.0 * std::sqrt(mu) + 4.0);
