@@ -286,9 +286,23 @@ int launch_rows(const T *x, int64_t rows, int cols, int64_t ld, const int32_t *r
                 int32_t *out, int64_t ld_out, cudaStream_t st) {
   if (warp_rows_fit(cols, K))
     return launch_warp<T, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out, ld_out, st);
-  if (short_cta_rows_fit<T>(cols, K))
-    return launch<T, kShortBlock, 512, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out, ld_out,
-                                                   st);
+  if (short_cta_rows_fit<T>(cols, K)) {
+    // above 16384 columns the 128-thread CTA pays through occupancy only: a
+    // batch that does not fill one wave of 256-thread CTAs keeps the wider
+    // CTA, whose extra threads shorten each row
+    bool use_short = cols <= 16384;
+    if (!use_short) {
+      auto wide = topk_rows_kernel<T, kBlock, 512, ALIGN, Out>;
+      const size_t smem = sizeof(ListSmem<kBlock, 512>);
+      if (allow_smem(wide, smem)) {
+        const int64_t wave = resident_ctas(reinterpret_cast<const void *>(wide), kBlock, smem);
+        use_short = wave > 0 && rows >= wave;
+      }
+    }
+    if (use_short)
+      return launch<T, kShortBlock, 512, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out,
+                                                     ld_out, st);
+  }
   if (K <= 1024)
     return launch_rows_cta<T, kBlock, 512, ALIGN, Out>(x, rows, cols, ld, row_ends, K, out,
                                                        ld_out, st);

@@ -92,6 +92,17 @@ def test_topk_shapes_both_paths(dtype, cols):
         assert_rows_equal(got, want, f"{dtype} cols={cols} k={k}")
 
 
+@pytest.mark.parametrize("dtype,cols", [(torch.float32, 20480), (torch.bfloat16, 30720)])
+def test_topk_short_cta_wide_rows_full_wave(dtype, cols):
+    """Rows of 16K-45K columns in a batch that fills a wave of CTAs take the
+    128-thread CTA (its list-fit rule); every row against the oracle."""
+    rows = 1024
+    x, ends = inputs.prefill(rows=rows, cols=cols, seed=cols + 11, dtype=dtype)
+    ends[:3] = torch.tensor([0, 700, cols], dtype=torch.int32)
+    got, want = run_topk(x, 512, ends, 512 + 7)
+    assert_rows_equal(got, want, f"{dtype} {rows}x{cols}")
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("cols,ld", [(3001, 3003), (20001, 20005), (777, 777)])
 def test_topk_unaligned_rows(dtype, cols, ld):
